@@ -1,0 +1,20 @@
+"""CPU oracle for the block-sparse fused LM-head (test infrastructure only).
+
+Plain, slow, obviously correct float64 NumPy restatements of what the path
+computes, written from "perf(megatron): add block-sparse fused LM-head
+backward" (SkyRL PR #2376; sections "What does this PR do?", "How it works",
+Bugbot "Overview") and the textbook definitions of log-softmax, softmax
+entropy and their gradients that the page names.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The GPU library never calls it.
+"""
+from .spans import active_spans, span_rows
+from .lmhead import (lmhead_forward, lmhead_forward_rows, lmhead_dlogits_rows,
+                     lmhead_backward, lmhead_backward_rows_weighted, loss_value)
+
+__all__ = [
+    "active_spans", "span_rows", "lmhead_forward", "lmhead_forward_rows",
+    "lmhead_dlogits_rows", "lmhead_backward", "lmhead_backward_rows_weighted",
+    "loss_value",
+]
