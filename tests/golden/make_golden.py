@@ -36,7 +36,7 @@ def main():
     with open(os.path.join(HERE, "tiny_fp32_forward.txt"), "w") as f:
         f.write("# tiny_fp32 workload (seed 1001): token logprob entropy lse (float64 oracle)\n")
         for i in range(len(lp)):
-            f.write(f"{i} {lp[i]!r} {ent[i]!r} {lse[i]!r}\n")
+            f.write(f"{i} {float(lp[i])!r} {float(ent[i])!r} {float(lse[i])!r}\n")
 
 
 if __name__ == "__main__":
