@@ -1,0 +1,669 @@
+// C ABI of the block-sparse fused LM-head (declared in include/eas.h).
+//
+// Host side only: argument checks, the workspace layout, TMA tensor maps, and
+// the stream-ordered launch sequence of each call.  No call allocates memory
+// or synchronises the host (except eas_read_device_status).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/eas.h"
+#include "eas_device.cuh"
+#include "eas_kernels.h"
+
+using namespace eas;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+eas_status fail(eas_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+eas_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(EAS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define EAS_CUDA(call, what)                  \
+  do {                                        \
+    cudaError_t e_ = (call);                  \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+  } while (0)
+
+inline long long round_up(long long x, long long m) { return (x + m - 1) / m * m; }
+inline long long cdiv(long long x, long long m) { return (x + m - 1) / m; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------ device info
+
+struct DevInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+
+eas_status device_info(DevInfo* out) {
+  static std::mutex mu;
+  static DevInfo cache[64];
+  static bool have[64] = {};
+  int dev = 0;
+  EAS_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(EAS_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (!have[dev]) {
+    DevInfo d;
+    EAS_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev), "sm count");
+    EAS_CUDA(cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev), "cc");
+    EAS_CUDA(cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev), "cc");
+    cache[dev] = d;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  if (out->major != 10 || out->minor != 3)
+    return fail(EAS_ERR_UNSUPPORTED, "built for sm_103a; device is sm_%d%d", out->major,
+                out->minor);
+  return EAS_OK;
+}
+
+long long wait_budget() {
+  static long long b = [] {
+    const char* s = getenv("EAS_WAIT_BUDGET_CYCLES");
+    long long v = s ? atoll(s) : 0;
+    return v > 0 ? v : (1LL << 31);   // ~1 s at 2 GHz
+  }();
+  return b;
+}
+
+// ------------------------------------------------------------ tracing
+//
+// When enabled, every kernel launch of the library is bracketed by a pair of
+// CUDA events on its stream, tagged with the kernel's kind; eas_trace_read()
+// returns the durations.  Off by default; meant for eager (not captured)
+// launches.
+
+enum TraceKind : int {
+  kTrSpans = 0, kTrRowmap, kTrGather, kTrFwdGemm, kTrCombine, kTrZeroRows,
+  kTrDLogitsGemm, kTrDHiddenGemm, kTrDWeightGemm, kTrSimtFwd, kTrSimtDLogits,
+  kTrSimtDHidden, kTrSimtDWeight, kTrMemset, kTrCount
+};
+
+const char* const kTraceNames[kTrCount] = {
+    "spans_build", "rowmap", "gather_rows", "fwd_gemm_tc", "combine", "zero_rows",
+    "dlogits_gemm_tc", "dhidden_gemm_tc", "dweight_gemm_tc", "fwd_gemm_simt",
+    "dlogits_gemm_simt", "dhidden_gemm_simt", "dweight_gemm_simt", "memset"};
+
+struct TraceRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace_pool;   // events are created once and reused
+size_t g_trace_used = 0;
+
+class Trace {
+ public:
+  Trace(int kind, cudaStream_t s) : s_(s) {
+    if (!g_trace_on) return;
+    std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (g_trace_used == g_trace_pool.size()) {
+      TraceRec r{kind, nullptr, nullptr};
+      if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+      g_trace_pool.push_back(r);
+    }
+    rec_ = &g_trace_pool[g_trace_used++];
+    rec_->kind = kind;
+    cudaEventRecord(rec_->a, s_);
+  }
+  ~Trace() {
+    if (rec_) cudaEventRecord(rec_->b, s_);
+  }
+
+ private:
+  cudaStream_t s_;
+  TraceRec* rec_ = nullptr;
+};
+
+// ------------------------------------------------------------ tensor maps
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+eas_status get_encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn f = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                           cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) f = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!f) return fail(EAS_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *fn = f;
+  return EAS_OK;
+}
+
+// 2-D bf16 tensor [rows][cols] with row pitch `ld` elements, 128-byte swizzle,
+// box of 64 columns x box_rows rows; out-of-range elements read as zero.
+eas_status make_map_bf16(CUtensorMap* m, const void* base, long long cols, long long rows,
+                         long long ld, int box_rows) {
+  EncodeTiledFn enc;
+  eas_status s = get_encoder(&enc);
+  if (s != EAS_OK) return s;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(EAS_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld] ld %lld",
+                static_cast<int>(r), rows, cols, ld);
+  return EAS_OK;
+}
+
+// ---------------------------------------------------------- workspace layout
+
+struct Layout {
+  long long T_pad;
+  int vt;              // vocabulary tile width of the forward partials
+  int n_vt;
+  long long vc;        // vocabulary chunk of the backward
+  int n_chunks;
+  long long ldz;       // staging row pitch (elements)
+  size_t status, sched, row_map, pack_of, hp;   // common part
+  size_t pm, ps, pu, zt;                          // forward part
+  size_t dz, acc;                                 // backward part
+  size_t fwd_end, bwd_end, total;
+};
+
+size_t align_up(size_t x) { return (x + 1023) / 1024 * 1024; }
+
+Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chunk) {
+  Layout L;
+  const size_t esz = (dt == EAS_BF16) ? 2 : 4;
+  L.T_pad = round_up(T, 128);
+  L.vt = (dt == EAS_BF16) ? kTcBN : kSimtBN;
+  L.n_vt = static_cast<int>(cdiv(V, L.vt));
+  if (chunk <= 0) chunk = EAS_DEFAULT_VOCAB_CHUNK;
+  L.vc = chunk < V ? chunk : V;
+  L.n_chunks = static_cast<int>(cdiv(V, L.vc));
+  L.ldz = (dt == EAS_BF16) ? round_up(L.vc, kTcBN) : round_up(L.vc, kSimtBN);
+  size_t o = 0;
+  L.status = o; o = align_up(o + sizeof(DevStatus));
+  L.sched = o; o = align_up(o + sizeof(Sched));
+  L.row_map = o; o = align_up(o + 4 * static_cast<size_t>(L.T_pad > 0 ? L.T_pad : 1));
+  L.pack_of = o; o = align_up(o + 4 * static_cast<size_t>(T > 0 ? T : 1));
+  L.hp = o; o = align_up(o + esz * static_cast<size_t>(L.T_pad) * H);
+  const size_t common = o;
+  L.pm = o; o = align_up(o + 4 * static_cast<size_t>(L.n_vt) * L.T_pad);
+  L.ps = o; o = align_up(o + 4 * static_cast<size_t>(L.n_vt) * L.T_pad);
+  L.pu = o; o = align_up(o + 4 * static_cast<size_t>(L.n_vt) * L.T_pad);
+  L.zt = o; o = align_up(o + 4 * static_cast<size_t>(L.T_pad));
+  L.fwd_end = o;
+  o = common;
+  L.dz = o; o = align_up(o + esz * static_cast<size_t>(L.T_pad) * L.ldz);
+  L.acc = o;
+  if (L.n_chunks > 1) o = align_up(o + 4 * static_cast<size_t>(L.T_pad) * H);
+  L.bwd_end = o;
+  L.total = L.fwd_end > L.bwd_end ? L.fwd_end : L.bwd_end;
+  return L;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+eas_status check_shape(long long T, long long H, long long V, eas_dtype dt) {
+  if (T < 0 || T > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "T=%lld out of range", T);
+  if (V < 1 || V > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "V=%lld out of range", V);
+  if (H < 1 || H > (1LL << 20)) return fail(EAS_ERR_INVALID_ARG, "H=%lld out of range", H);
+  if (dt != EAS_BF16 && dt != EAS_FP32) return fail(EAS_ERR_INVALID_ARG, "dtype %d", (int)dt);
+  if (dt == EAS_BF16 && H % 64 != 0)
+    return fail(EAS_ERR_UNSUPPORTED, "bf16 path needs H %% 64 == 0 (H=%lld)", H);
+  if (dt == EAS_FP32 && H % 4 != 0)
+    return fail(EAS_ERR_UNSUPPORTED, "fp32 path needs H %% 4 == 0 (H=%lld)", H);
+  return EAS_OK;
+}
+
+// Common prologue of forward and backward: status clear, span validation and
+// row schedule, packed copy of hidden.
+eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* spans,
+                    const int32_t* num_spans, int64_t cap, long long T, long long H,
+                    eas_dtype dt, uint32_t flags, void* ws, const Layout& L, const DevInfo& di,
+                    cudaStream_t s) {
+  {
+    Trace tr_(kTrMemset, s);
+    EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, 2 * 1024, s), "clear status");
+  }
+  if (T == 0) return EAS_OK;
+  {
+    Trace tr_(kTrRowmap, s);
+    EAS_CUDA(launch_rowmap(mask, spans, num_spans, cap, T, (flags & EAS_ROWS_SPAN) ? 1 : 0,
+                           at<int>(ws, L.row_map), at<int>(ws, L.pack_of), at<Sched>(ws, L.sched),
+                           at<DevStatus>(ws, L.status), s),
+             "rowmap");
+  }
+  const long long row_bytes = H * ((dt == EAS_BF16) ? 2 : 4);
+  {
+    Trace tr_(kTrGather, s);
+    EAS_CUDA(launch_gather_rows(hidden, at<char>(ws, L.hp), at<int>(ws, L.row_map),
+                                at<Sched>(ws, L.sched), L.T_pad, row_bytes, di.sms, s),
+             "gather");
+  }
+  return EAS_OK;
+}
+
+int group_for(long long bytes_per_mtile, long long num_m) {
+  const long long budget = 48LL << 20;
+  long long g = bytes_per_mtile > 0 ? budget / bytes_per_mtile : num_m;
+  if (g < 1) g = 1;
+  if (g > num_m) g = num_m;
+  return static_cast<int>(g > 0 ? g : 1);
+}
+
+int grid_for(long long tiles, int sms) {
+  return static_cast<int>(tiles < sms ? tiles : sms);
+}
+
+}  // namespace
+
+// =====================================================================
+extern "C" {
+
+size_t eas_spans_workspace_size(int64_t T) {
+  (void)T;
+  return 1024;
+}
+
+eas_status eas_build_active_spans(const uint8_t* mask, int64_t T, int32_t max_gap,
+                                  int32_t* spans, int64_t cap, int32_t* num_spans, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  if (T < 0 || T > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "T=%lld out of range", (long long)T);
+  if (max_gap < 0) return fail(EAS_ERR_INVALID_ARG, "max_gap must be >= 0");
+  if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
+  if (!num_spans || (T > 0 && !mask) || (cap > 0 && !spans))
+    return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (!ws || ws_bytes < eas_spans_workspace_size(T)) return fail(EAS_ERR_WORKSPACE, "workspace too small");
+  if (!aligned(ws, 16)) return fail(EAS_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  DevInfo di;
+  eas_status st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    Trace tr_(kTrMemset, s);
+    EAS_CUDA(cudaMemsetAsync(ws, 0, sizeof(DevStatus), s), "clear status");
+  }
+  {
+    Trace tr_(kTrSpans, s);
+    EAS_CUDA(launch_spans_build(mask, T, max_gap, spans, cap, num_spans, static_cast<DevStatus*>(ws), s),
+             "spans_build");
+  }
+  return EAS_OK;
+}
+
+size_t eas_lmhead_workspace_size(int64_t T, int64_t H, int64_t V, eas_dtype dtype,
+                                 int64_t vocab_chunk) {
+  if (T < 0 || H < 1 || V < 1) return 0;
+  return layout(T, H, V, dtype, vocab_chunk).total;
+}
+
+eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t* targets,
+                          const uint8_t* mask, const int32_t* spans, const int32_t* num_spans,
+                          int64_t cap, int64_t T, int64_t H, int64_t V, eas_dtype dtype,
+                          uint32_t flags, float* logprob, float* entropy, float* lse, void* ws,
+                          size_t ws_bytes, void* stream) {
+  eas_status st = check_shape(T, H, V, dtype);
+  if (st != EAS_OK) return st;
+  if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
+  if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
+  if (!weight || !num_spans || !ws) return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (T > 0 && (!hidden || !targets || !mask || !logprob || !entropy || !lse || (cap > 0 && !spans)))
+    return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(ws, 256))
+    return fail(EAS_ERR_INVALID_ARG, "hidden/weight must be 16-byte and ws 256-byte aligned");
+  const Layout L = layout(T, H, V, dtype, 0);
+  if (ws_bytes < L.fwd_end) return fail(EAS_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, L.fwd_end);
+  DevInfo di;
+  st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, ws, L, di, s);
+  if (st != EAS_OK || T == 0) return st;
+  const Sched* sched = at<Sched>(ws, L.sched);
+  const long long num_m_max = L.T_pad / 128;
+
+  if (dtype == EAS_BF16) {
+    TcArgs a;
+    memset(&a, 0, sizeof(a));
+    st = make_map_bf16(&a.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128);
+    if (st != EAS_OK) return st;
+    st = make_map_bf16(&a.tmB, weight, H, V, H, 256);
+    if (st != EAS_OK) return st;
+    a.sched = sched;
+    a.status = at<DevStatus>(ws, L.status);
+    a.budget = wait_budget();
+    a.kind = kTcFwd;
+    a.M_fixed = 0;
+    a.N = static_cast<int>(V);
+    a.K_fixed = static_cast<int>(H);
+    a.group_m = group_for(128LL * H * 2, num_m_max);
+    a.v0 = 0;
+    a.row_map = at<int>(ws, L.row_map);
+    a.targets = targets;
+    a.part_m = at<float>(ws, L.pm);
+    a.part_s = at<float>(ws, L.ps);
+    a.part_u = at<float>(ws, L.pu);
+    a.zt = at<float>(ws, L.zt);
+    a.part_stride = L.T_pad;
+    a.V = static_cast<int>(V);
+    a.H = static_cast<int>(H);
+    {
+      Trace tr_(kTrFwdGemm, s);
+      EAS_CUDA(launch_tc_gemm(a, grid_for(num_m_max * L.n_vt, di.sms), s), "fwd gemm");
+    }
+  } else {
+    SimtArgs a;
+    memset(&a, 0, sizeof(a));
+    a.kind = kTcFwd;
+    a.A = at<float>(ws, L.hp);
+    a.lda = H;
+    a.B = static_cast<const float*>(weight);
+    a.ldb = H;
+    a.sched = sched;
+    a.M_fixed = 0;
+    a.N = static_cast<int>(V);
+    a.K_fixed = static_cast<int>(H);
+    a.row_map = at<int>(ws, L.row_map);
+    a.targets = targets;
+    a.part_m = at<float>(ws, L.pm);
+    a.part_s = at<float>(ws, L.ps);
+    a.part_u = at<float>(ws, L.pu);
+    a.zt = at<float>(ws, L.zt);
+    a.part_stride = L.T_pad;
+    a.V = static_cast<int>(V);
+    a.H = static_cast<int>(H);
+    {
+      Trace tr_(kTrSimtFwd, s);
+      EAS_CUDA(launch_simt_gemm(a, cdiv(L.T_pad, kSimtBM) * L.n_vt, s), "fwd simt");
+    }
+  }
+  {
+    Trace tr_(kTrCombine, s);
+    EAS_CUDA(launch_combine(at<float>(ws, L.pm), at<float>(ws, L.ps), at<float>(ws, L.pu),
+                            at<float>(ws, L.zt), L.n_vt, L.T_pad, at<int>(ws, L.pack_of), mask, T,
+                            logprob, entropy, lse, di.sms, s),
+             "combine");
+  }
+  return EAS_OK;
+}
+
+eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const void* hidden,
+                          const void* weight, const int32_t* targets, const uint8_t* mask,
+                          const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                          const float* lse, const float* entropy, int64_t T, int64_t H, int64_t V,
+                          eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
+                          float* dweight, void* ws, size_t ws_bytes, void* stream) {
+  eas_status st = check_shape(T, H, V, dtype);
+  if (st != EAS_OK) return st;
+  if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
+  if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
+  if (vocab_chunk < 0) return fail(EAS_ERR_INVALID_ARG, "vocab_chunk must be >= 0");
+  if (!weight || !dweight || !num_spans || !ws) return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (T > 0 && (!hidden || !targets || !mask || !g_logprob || !g_entropy || !lse || !entropy ||
+                !dhidden || (cap > 0 && !spans)))
+    return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(dhidden, 16) ||
+      !aligned(dweight, 16) || !aligned(ws, 256))
+    return fail(EAS_ERR_INVALID_ARG, "tensors must be 16-byte and ws 256-byte aligned");
+  const Layout L = layout(T, H, V, dtype, vocab_chunk);
+  if (ws_bytes < L.bwd_end) return fail(EAS_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, L.bwd_end);
+  DevInfo di;
+  st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, ws, L, di, s);
+  if (st != EAS_OK) return st;
+  if (T == 0) {
+    {
+      Trace tr_(kTrMemset, s);
+      EAS_CUDA(cudaMemsetAsync(dweight, 0, sizeof(float) * V * H, s), "zero dW");
+    }
+    return EAS_OK;
+  }
+  const size_t esz = (dtype == EAS_BF16) ? 2 : 4;
+  {
+    Trace tr_(kTrZeroRows, s);
+    EAS_CUDA(launch_zero_unpacked_rows(dhidden, at<int>(ws, L.pack_of), T, H * esz, di.sms, s),
+             "zero rows");
+  }
+  const Sched* sched = at<Sched>(ws, L.sched);
+  const long long num_m_max = L.T_pad / 128;
+
+  if (dtype == EAS_BF16) {
+    CUtensorMap hp_k, w_k, w_mn, hp_mn;
+    if ((st = make_map_bf16(&hp_k, at<char>(ws, L.hp), H, L.T_pad, H, 128)) != EAS_OK) return st;
+    if ((st = make_map_bf16(&w_k, weight, H, V, H, 256)) != EAS_OK) return st;
+    if ((st = make_map_bf16(&w_mn, weight, H, V, H, 64)) != EAS_OK) return st;
+    if ((st = make_map_bf16(&hp_mn, at<char>(ws, L.hp), H, L.T_pad, H, 64)) != EAS_OK) return st;
+    TcArgs base;
+    memset(&base, 0, sizeof(base));
+    base.sched = sched;
+    base.status = at<DevStatus>(ws, L.status);
+    base.budget = wait_budget();
+    base.row_map = at<int>(ws, L.row_map);
+    base.targets = targets;
+    base.mask = mask;
+    base.lse = lse;
+    base.ent = entropy;
+    base.g_lp = g_logprob;
+    base.g_h = g_entropy;
+    base.V = static_cast<int>(V);
+    base.H = static_cast<int>(H);
+    base.dz = at<char>(ws, L.dz);
+    base.ldz = L.ldz;
+    base.acc = at<float>(ws, L.acc);
+    base.dhidden = dhidden;
+    base.dW = dweight;
+    for (int c = 0; c < L.n_chunks; ++c) {
+      const long long v0 = c * L.vc;
+      const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
+      // d-logits of the active rows, this chunk's live columns only
+      TcArgs a = base;
+      a.tmA = hp_k;
+      a.tmB = w_k;
+      a.kind = kTcDLogits;
+      a.M_fixed = 0;
+      a.N = static_cast<int>(live);
+      a.K_fixed = static_cast<int>(H);
+      a.group_m = group_for(128LL * H * 2, num_m_max);
+      a.v0 = static_cast<int>(v0);
+      a.vc_live = static_cast<int>(live);
+      {
+        Trace tr_(kTrDLogitsGemm, s);
+        EAS_CUDA(launch_tc_gemm(a, grid_for(num_m_max * cdiv(live, kTcBN), di.sms), s), "dlogits");
+      }
+      CUtensorMap dz_k, dz_mn;
+      if ((st = make_map_bf16(&dz_k, base.dz, live, L.T_pad, L.ldz, 128)) != EAS_OK) return st;
+      if ((st = make_map_bf16(&dz_mn, base.dz, live, L.T_pad, L.ldz, 64)) != EAS_OK) return st;
+      // dHidden of the packed rows
+      TcArgs h = base;
+      h.tmA = dz_k;
+      h.tmB = w_mn;
+      h.kind = kTcDHidden;
+      h.M_fixed = 0;
+      h.N = static_cast<int>(H);
+      h.K_fixed = static_cast<int>(live);
+      h.group_m = group_for(128LL * live * 2, num_m_max);
+      h.v0 = static_cast<int>(v0);
+      h.vc_live = static_cast<int>(live);
+      h.first_chunk = (c == 0);
+      h.last_chunk = (c == L.n_chunks - 1);
+      {
+        Trace tr_(kTrDHiddenGemm, s);
+        EAS_CUDA(launch_tc_gemm(h, grid_for(num_m_max * cdiv(H, kTcBN), di.sms), s), "dhidden");
+      }
+      // dW rows of this chunk
+      TcArgs w = base;
+      w.tmA = dz_mn;
+      w.tmB = hp_mn;
+      w.kind = kTcDWeight;
+      w.M_fixed = static_cast<int>(live);
+      w.N = static_cast<int>(H);
+      w.K_fixed = 0;
+      w.group_m = group_for(128LL * L.T_pad * 2, cdiv(live, kTcBM));
+      w.v0 = static_cast<int>(v0);
+      w.vc_live = static_cast<int>(live);
+      {
+        Trace tr_(kTrDWeightGemm, s);
+        EAS_CUDA(launch_tc_gemm(w, grid_for(cdiv(live, kTcBM) * cdiv(H, kTcBN), di.sms), s), "dweight");
+      }
+    }
+  } else {
+    SimtArgs base;
+    memset(&base, 0, sizeof(base));
+    base.sched = sched;
+    base.row_map = at<int>(ws, L.row_map);
+    base.targets = targets;
+    base.mask = mask;
+    base.lse = lse;
+    base.ent = entropy;
+    base.g_lp = g_logprob;
+    base.g_h = g_entropy;
+    base.V = static_cast<int>(V);
+    base.H = static_cast<int>(H);
+    base.dz = at<float>(ws, L.dz);
+    base.ldz = L.ldz;
+    base.acc = at<float>(ws, L.acc);
+    base.dhidden = static_cast<float*>(dhidden);
+    base.dW = dweight;
+    for (int c = 0; c < L.n_chunks; ++c) {
+      const long long v0 = c * L.vc;
+      const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
+      SimtArgs a = base;
+      a.kind = kTcDLogits;
+      a.A = at<float>(ws, L.hp);
+      a.lda = H;
+      a.B = static_cast<const float*>(weight);
+      a.ldb = H;
+      a.M_fixed = 0;
+      a.N = static_cast<int>(live);
+      a.K_fixed = static_cast<int>(H);
+      a.v0 = static_cast<int>(v0);
+      a.vc_live = static_cast<int>(live);
+      {
+        Trace tr_(kTrSimtDLogits, s);
+        EAS_CUDA(launch_simt_gemm(a, cdiv(L.T_pad, kSimtBM) * cdiv(live, kSimtBN), s), "dlogits simt");
+      }
+      SimtArgs h = base;
+      h.kind = kTcDHidden;
+      h.A = at<float>(ws, L.dz);
+      h.lda = L.ldz;
+      h.B = static_cast<const float*>(weight);
+      h.ldb = H;
+      h.M_fixed = 0;
+      h.N = static_cast<int>(H);
+      h.K_fixed = static_cast<int>(live);
+      h.v0 = static_cast<int>(v0);
+      h.vc_live = static_cast<int>(live);
+      h.first_chunk = (c == 0);
+      h.last_chunk = (c == L.n_chunks - 1);
+      {
+        Trace tr_(kTrSimtDHidden, s);
+        EAS_CUDA(launch_simt_gemm(h, cdiv(L.T_pad, kSimtBM) * cdiv(H, kSimtBN), s), "dhidden simt");
+      }
+      SimtArgs w = base;
+      w.kind = kTcDWeight;
+      w.A = at<float>(ws, L.dz);
+      w.lda = L.ldz;
+      w.B = at<float>(ws, L.hp);
+      w.ldb = H;
+      w.M_fixed = static_cast<int>(live);
+      w.N = static_cast<int>(H);
+      w.K_fixed = 0;
+      w.v0 = static_cast<int>(v0);
+      w.vc_live = static_cast<int>(live);
+      {
+        Trace tr_(kTrSimtDWeight, s);
+        EAS_CUDA(launch_simt_gemm(w, cdiv(live, kSimtBM) * cdiv(H, kSimtBN), s), "dweight simt");
+      }
+    }
+  }
+  return EAS_OK;
+}
+
+eas_status eas_read_device_status(const void* ws, void* stream) {
+  if (!ws) return fail(EAS_ERR_INVALID_ARG, "null workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  DevStatus h;
+  EAS_CUDA(cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, s), "read status");
+  EAS_CUDA(cudaStreamSynchronize(s), "stream sync");
+  if (h.code != 0)
+    return fail(static_cast<eas_status>(h.code), "device status %d (where %d, info %d)", h.code,
+                h.where, h.info);
+  return EAS_OK;
+}
+
+void eas_trace_enable(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  g_trace_on = (on != 0);
+  if (g_trace_on) g_trace_used = 0;
+}
+
+int32_t eas_trace_read(int32_t* kinds, float* ms, int32_t cap) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  const int32_t n = static_cast<int32_t>(g_trace_used);
+  for (int32_t i = 0; i < n && i < cap; ++i) {
+    const TraceRec& r = g_trace_pool[i];
+    float t = -1.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess)
+      t = -1.f;
+    if (kinds) kinds[i] = r.kind;
+    if (ms) ms[i] = t;
+  }
+  return n;
+}
+
+const char* eas_kernel_name(int32_t kind) {
+  return (kind >= 0 && kind < kTrCount) ? kTraceNames[kind] : "unknown";
+}
+
+const char* eas_last_error(void) { return g_err; }
+
+const char* eas_status_string(eas_status s) {
+  switch (s) {
+    case EAS_OK: return "EAS_OK";
+    case EAS_ERR_INVALID_ARG: return "EAS_ERR_INVALID_ARG";
+    case EAS_ERR_INVALID_SPANS: return "EAS_ERR_INVALID_SPANS";
+    case EAS_ERR_UNSUPPORTED: return "EAS_ERR_UNSUPPORTED";
+    case EAS_ERR_WORKSPACE: return "EAS_ERR_WORKSPACE";
+    case EAS_ERR_CUDA: return "EAS_ERR_CUDA";
+    case EAS_ERR_TIMEOUT: return "EAS_ERR_TIMEOUT";
+    case EAS_ERR_SPAN_CAPACITY: return "EAS_ERR_SPAN_CAPACITY";
+  }
+  return "EAS_UNKNOWN";
+}
+
+int32_t eas_version(void) { return 100; }
+
+}  // extern "C"

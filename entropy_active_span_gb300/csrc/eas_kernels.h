@@ -1,0 +1,121 @@
+// Internal launchers shared by the C-ABI layer (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace eas {
+
+struct DevStatus;
+struct Sched;
+
+// ---- span builder and row schedule (eas_sched.cu) ----
+cudaError_t launch_spans_build(const uint8_t* mask, long long T, int max_gap, int* spans,
+                               long long cap, int* num_spans, DevStatus* st, cudaStream_t s);
+cudaError_t launch_rowmap(const uint8_t* mask, const int* spans, const int* num_spans,
+                          long long cap, long long T, int span_rows, int* row_map, int* pack_of,
+                          Sched* sched, DevStatus* st, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* src, void* dst, const int* row_map, const Sched* sched,
+                               long long T_pad, long long row_bytes, int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, const float* zt,
+                           int n_tiles, long long stride, const int* pack_of, const uint8_t* mask,
+                           long long T, float* logprob, float* entropy, float* lse, int num_sms,
+                           cudaStream_t s);
+cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T,
+                                      long long row_bytes, int num_sms, cudaStream_t s);
+
+// ---- tcgen05 GEMMs with fused epilogues, bf16 (eas_gemm_tc.cu) ----
+
+// Tile shape of every tensor-core GEMM: 128 x 256 accumulator in TMEM, K in
+// blocks of 64 bf16 (one 128-byte swizzle row).
+constexpr int kTcBM = 128;
+constexpr int kTcBN = 256;
+constexpr int kTcBK = 64;
+
+enum TcKind : int {
+  kTcFwd = 0,      // Z = Hp W^T -> per-tile softmax partials (+ target logit)
+  kTcDLogits = 1,  // Z = Hp W_c^T -> dZ_c (bf16 staging)
+  kTcDHidden = 2,  // dHacc (+)= dZ_c W_c -> fp32 accumulator / final dhidden
+  kTcDWeight = 3,  // dW_c = dZ_c^T Hp -> fp32 dW rows
+};
+
+struct TcArgs {
+  CUtensorMap tmA;   // A operand (see TcKind for the layout of each kind)
+  CUtensorMap tmB;   // B operand
+  const void* sched; // Sched*: packed row count R, R_pad
+  void* status;      // DevStatus*
+  long long budget;  // clocks before a pipeline wait gives up
+  int kind;
+  int M_fixed;       // > 0: rows of the problem; 0: R_pad from sched
+  int N;             // columns of the problem
+  int K_fixed;       // > 0: reduction length; 0: R_pad from sched
+  int group_m;       // m-tiles per raster band
+  int v0;            // first vocabulary row of the chunk (B row / k offset)
+  // epilogue operands
+  const int* row_map;     // packed row -> token (or -1)
+  const int* targets;     // [T]
+  const uint8_t* mask;    // [T]
+  const float* lse;       // [T]
+  const float* ent;       // [T]
+  const float* g_lp;      // [T]
+  const float* g_h;       // [T]
+  float* part_m;          // fwd partials, [n_vtiles][stride]
+  float* part_s;
+  float* part_u;
+  float* zt;              // [stride]
+  long long part_stride;
+  int V;                  // vocabulary size (fwd column bound)
+  int vc_live;            // live columns of this chunk (dlogits / dweight)
+  void* dz;               // bf16 staging [T_pad][ldz]
+  long long ldz;
+  float* acc;             // fp32 dHidden accumulator [T_pad][H]
+  void* dhidden;          // bf16 [T][H]
+  int H;
+  int first_chunk;
+  int last_chunk;
+  float* dW;              // fp32 [V][H]
+};
+
+size_t tc_smem_bytes();
+cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s);
+
+// ---- fp32 SIMT GEMMs with the same epilogues (eas_simt.cu) ----
+constexpr int kSimtBM = 64;
+constexpr int kSimtBN = 64;
+
+struct SimtArgs {
+  int kind;               // TcKind values
+  const float* A;         // see launch_simt_gemm
+  const float* B;
+  long long lda, ldb;
+  const void* sched;
+  int M_fixed, N, K_fixed;
+  int v0;
+  const int* row_map;
+  const int* targets;
+  const uint8_t* mask;
+  const float* lse;
+  const float* ent;
+  const float* g_lp;
+  const float* g_h;
+  float* part_m;
+  float* part_s;
+  float* part_u;
+  float* zt;
+  long long part_stride;
+  int V;
+  int vc_live;
+  float* dz;
+  long long ldz;
+  float* acc;
+  float* dhidden;
+  int H;
+  int first_chunk;
+  int last_chunk;
+  float* dW;
+};
+
+cudaError_t launch_simt_gemm(const SimtArgs& args, long long max_tiles, cudaStream_t s);
+
+}  // namespace eas

@@ -1,0 +1,379 @@
+// Span builder and row schedule ("perf(megatron): add block-sparse fused
+// LM-head backward", SkyRL PR #2376: "What does this PR do?" - ordered active
+// spans; Bugbot "Overview" - spans coalesced with gaps <= 128; "How it works" -
+// spans are used without reordering tokens).
+//
+// The page builds spans on the host before the device copy; here they are
+// built on the device (edge detection + block scans + stream compaction), so a
+// training step never waits on the host and the calls can be graph-captured.
+//
+// Kernels:
+//   spans_build_kernel   mask -> spans[S][2], S                 (one CTA)
+//   rowmap_kernel        spans + mask -> validated row schedule (one CTA)
+//   gather_rows_kernel   hidden rows of the schedule -> packed copy
+//   combine_kernel       per-vocab-tile softmax partials -> lse, entropy, logp
+//   zero_unpacked_rows_kernel  dhidden rows that no GEMM tile writes -> 0
+#include "eas_device.cuh"
+#include "eas_kernels.h"
+
+namespace eas {
+
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 16;
+constexpr int kScanWarps = kScanThreads / 32;
+
+// Block-wide exclusive sum (and the block total) of one int per thread.
+__device__ __forceinline__ int block_excl_sum(int v, int* sm, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < kScanWarps) ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sm[lane] = w;
+  }
+  __syncthreads();
+  const int before = warp ? sm[warp - 1] : 0;
+  total = sm[kScanWarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+// Block-wide exclusive max (identity -1) and the block maximum.
+__device__ __forceinline__ long long block_excl_max(long long v, long long* sm, long long& all) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x = max(x, y);
+  }
+  long long excl = __shfl_up_sync(0xffffffffu, x, 1);
+  if (lane == 0) excl = -1;
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = (lane < kScanWarps) ? sm[lane] : -1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w = max(w, y);
+    }
+    sm[lane] = w;
+  }
+  __syncthreads();
+  const long long before = warp ? sm[warp - 1] : -1;
+  all = sm[kScanWarps - 1];
+  __syncthreads();
+  return max(before, excl);
+}
+
+}  // namespace
+
+// One CTA walks the mask in tiles of kScanThreads * kScanItems tokens.  A token
+// t starts a span when it is active and the previous active token p is absent
+// or more than max_gap tokens away (t - p - 1 > max_gap); at that point the
+// previous span ends at p + 1.  The last span ends after the last active token.
+__global__ void __launch_bounds__(kScanThreads)
+spans_build_kernel(const uint8_t* __restrict__ mask, long long T, int max_gap,
+                   int* __restrict__ spans, long long cap, int* __restrict__ num_spans,
+                   DevStatus* st) {
+  __shared__ int sm_i[32];
+  __shared__ long long sm_l[32];
+  long long carry_last = -1;   // last active token before the current tile
+  long long carry_count = 0;   // spans started before the current tile
+  const long long tile = static_cast<long long>(kScanThreads) * kScanItems;
+  for (long long base = 0; base < T; base += tile) {
+    const long long t0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      const long long t = t0 + i;
+      if (t < T && mask[t] != 0) bits |= 1u << i;
+    }
+    long long my_last = -1;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i)
+      if (bits & (1u << i)) my_last = t0 + i;
+    long long tile_max;
+    long long prev = block_excl_max(my_last, sm_l, tile_max);
+    prev = max(prev, carry_last);
+    int cnt = 0;
+    uint32_t starts = 0;
+    long long p = prev;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      if (bits & (1u << i)) {
+        const long long t = t0 + i;
+        if (p < 0 || t - p - 1 > static_cast<long long>(max_gap)) {
+          starts |= 1u << i;
+          ++cnt;
+        }
+        p = t;
+      }
+    }
+    int total;
+    const int excl = block_excl_sum(cnt, sm_i, total);
+    long long k = carry_count + excl;
+    p = prev;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      if (bits & (1u << i)) {
+        const long long t = t0 + i;
+        if (starts & (1u << i)) {
+          if (k < cap) spans[2 * k] = static_cast<int>(t);
+          if (k >= 1 && k - 1 < cap) spans[2 * (k - 1) + 1] = static_cast<int>(p + 1);
+          ++k;
+        }
+        p = t;
+      }
+    }
+    carry_count += total;
+    carry_last = max(carry_last, tile_max);
+  }
+  if (threadIdx.x == 0) {
+    if (carry_count > 0 && carry_count - 1 < cap)
+      spans[2 * (carry_count - 1) + 1] = static_cast<int>(carry_last + 1);
+    *num_spans = static_cast<int>(carry_count);
+    if (carry_count > cap) report(st, kStSpanCapacity, 1, static_cast<int>(carry_count));
+  }
+}
+
+// Validates the spans and lists the rows the kernels work on, in span order:
+//   row_map[r] = token of packed row r (r < R), -1 for r in [R, R_pad);
+//   pack_of[t] = packed row of token t, or -1.
+// A row is listed when it lies in a span and (policy EAS_ROWS_SPAN, or the
+// token is active).  Spans must be sorted, disjoint, inside [0, T) and cover
+// every active token; otherwise nothing is listed (R = 0) and the status word
+// reads kStInvalidSpans.
+__global__ void __launch_bounds__(kScanThreads)
+rowmap_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
+              const int* __restrict__ num_spans, long long cap, long long T, int span_rows,
+              int* __restrict__ row_map, int* __restrict__ pack_of, Sched* sched,
+              DevStatus* st) {
+  __shared__ int sm_i[32];
+  __shared__ int bad;
+  const int S_raw = *num_spans;
+  if (threadIdx.x == 0) bad = 0;
+  __syncthreads();
+  int S = S_raw;
+  if (S_raw < 0 || static_cast<long long>(S_raw) > cap) {
+    if (threadIdx.x == 0) {
+      report(st, S_raw < 0 ? kStInvalidSpans : kStSpanCapacity, 2, S_raw);
+      bad = 1;
+    }
+    S = 0;
+  }
+  for (int k = threadIdx.x; k < S; k += kScanThreads) {
+    const int s = spans[2 * k], e = spans[2 * k + 1];
+    bool ok = (s >= 0) && (s < e) && (static_cast<long long>(e) <= T);
+    if (k > 0) ok = ok && (spans[2 * k - 1] <= s);
+    if (!ok) bad = 1;
+  }
+  __syncthreads();
+  if (bad) S = 0;
+
+  long long R = 0;
+  const long long tile = static_cast<long long>(kScanThreads) * kScanItems;
+  for (long long base = 0; base < T; base += tile) {
+    const long long t0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
+    // largest k with start_k <= t0 (or -1)
+    int lo = 0, hi = S;  // search in [lo, hi)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<long long>(spans[2 * mid]) <= t0) lo = mid + 1; else hi = mid;
+    }
+    int k = lo - 1;
+    uint32_t sel = 0;
+    int cnt = 0;
+    bool uncovered = false;
+#pragma unroll 4
+    for (int i = 0; i < kScanItems; ++i) {
+      const long long t = t0 + i;
+      if (t >= T) break;
+      while (k + 1 < S && static_cast<long long>(spans[2 * (k + 1)]) <= t) ++k;
+      const bool covered = (k >= 0) && (t < static_cast<long long>(spans[2 * k + 1]));
+      const bool active = mask[t] != 0;
+      if (active && !covered) uncovered = true;
+      if (covered && (span_rows || active)) {
+        sel |= 1u << i;
+        ++cnt;
+      }
+    }
+    if (uncovered) bad = 1;
+    int total;
+    const int excl = block_excl_sum(cnt, sm_i, total);
+    long long idx = R + excl;
+    for (int i = 0; i < kScanItems; ++i) {
+      const long long t = t0 + i;
+      if (t >= T) break;
+      if (sel & (1u << i)) {
+        row_map[idx] = static_cast<int>(t);
+        pack_of[t] = static_cast<int>(idx);
+        ++idx;
+      } else {
+        pack_of[t] = -1;
+      }
+    }
+    R += total;
+  }
+  __syncthreads();
+  if (bad) {
+    for (long long t = threadIdx.x; t < T; t += kScanThreads) pack_of[t] = -1;
+    if (threadIdx.x == 0) {
+      report(st, kStInvalidSpans, 2, -1);
+      sched->R = 0;
+      sched->R_pad = 0;
+      sched->S = S_raw;
+    }
+    return;
+  }
+  const long long R_pad = (R + 127) / 128 * 128;
+  for (long long r = R + threadIdx.x; r < R_pad; r += kScanThreads) row_map[r] = -1;
+  if (threadIdx.x == 0) {
+    sched->R = static_cast<int>(R);
+    sched->R_pad = static_cast<int>(R_pad);
+    sched->S = S_raw;
+  }
+}
+
+// dst[r, :] = src[row_map[r], :] for r < R_pad (zeros for pad rows).  One
+// 16-byte vector per thread per step; `vec_per_row` = H * sizeof(elem) / 16.
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                   const int* __restrict__ row_map, const Sched* __restrict__ sched,
+                   long long vec_per_row) {
+  const int R_pad = sched->R_pad;
+  for (long long r = blockIdx.x; r < R_pad; r += gridDim.x) {
+    const int t = row_map[r];
+    uint4* d = dst + r * vec_per_row;
+    if (t < 0) {
+      for (long long i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = make_uint4(0, 0, 0, 0);
+    } else {
+      const uint4* s = src + static_cast<long long>(t) * vec_per_row;
+      for (long long i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = __ldg(s + i);
+    }
+  }
+}
+
+// Folds the per-vocab-tile partials of each packed row into lse, entropy and
+// logp.  Partials are kept in base-2 units: with y = z log2(e), partial n of
+// row r holds, over the tile's valid columns, m = max y, s = sum 2^(y - m),
+// u = sum 2^(y - m) (y - m).  Merged in tile order:
+//   M = max m_n, S = sum s_n 2^(m_n - M), U = sum 2^(m_n - M) (u_n + (m_n - M) s_n)
+// so S = sum_v exp(z_v - M ln2) and U ln2 = sum_v exp(z_v - M ln2) (z_v - M ln2):
+//   lse = M ln2 + log S,  H = log S - (U / S) ln2,  logp = z_target - lse.
+// Tokens without a packed row, or with mask 0, get zeros.
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+               const float* __restrict__ pu, const float* __restrict__ zt, int n_tiles,
+               long long stride, const int* __restrict__ pack_of, const uint8_t* __restrict__ mask,
+               long long T, float* __restrict__ logprob, float* __restrict__ entropy,
+               float* __restrict__ lse) {
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < T;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int r = pack_of[t];
+    if (r < 0 || mask[t] == 0) {
+      logprob[t] = 0.f;
+      entropy[t] = 0.f;
+      lse[t] = 0.f;
+      continue;
+    }
+    float M = pm[r], S = ps[r], U = pu[r];
+    for (int n = 1; n < n_tiles; ++n) {
+      const float m = pm[n * stride + r];
+      const float s = ps[n * stride + r];
+      const float u = pu[n * stride + r];
+      if (m > M) {
+        const float d = M - m;                 // < 0
+        const float f = ex2_approx(d);
+        U = f * (U + d * S) + u;
+        S = f * S + s;
+        M = m;
+      } else {
+        const float d = m - M;                 // <= 0
+        const float f = ex2_approx(d);
+        S += f * s;
+        U += f * (u + d * s);
+      }
+    }
+    const float logS = logf(S);
+    const float l = fmaf(M, kLn2, logS);
+    lse[t] = l;
+    entropy[t] = logS - (U / S) * kLn2;
+    logprob[t] = zt[r] - l;
+  }
+}
+
+// Rows of dhidden that no GEMM tile writes (tokens outside the row schedule)
+// are set to zero.  `vec_per_row` 16-byte vectors per row.
+__global__ void __launch_bounds__(256)
+zero_unpacked_rows_kernel(uint4* __restrict__ out, const int* __restrict__ pack_of, long long T,
+                          long long vec_per_row) {
+  for (long long t = blockIdx.x; t < T; t += gridDim.x) {
+    if (pack_of[t] >= 0) continue;
+    uint4* d = out + t * vec_per_row;
+    for (long long i = threadIdx.x; i < vec_per_row; i += blockDim.x) d[i] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// ------------------------------------------------------------ launchers --
+
+cudaError_t launch_spans_build(const uint8_t* mask, long long T, int max_gap, int* spans,
+                               long long cap, int* num_spans, DevStatus* st, cudaStream_t s) {
+  spans_build_kernel<<<1, kScanThreads, 0, s>>>(mask, T, max_gap, spans, cap, num_spans, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rowmap(const uint8_t* mask, const int* spans, const int* num_spans,
+                          long long cap, long long T, int span_rows, int* row_map, int* pack_of,
+                          Sched* sched, DevStatus* st, cudaStream_t s) {
+  rowmap_kernel<<<1, kScanThreads, 0, s>>>(mask, spans, num_spans, cap, T, span_rows, row_map,
+                                           pack_of, sched, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* src, void* dst, const int* row_map, const Sched* sched,
+                               long long T_pad, long long row_bytes, int num_sms, cudaStream_t s) {
+  if (T_pad == 0) return cudaSuccess;
+  const long long grid = T_pad < 8LL * num_sms ? T_pad : 8LL * num_sms;
+  gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
+      static_cast<const uint4*>(src), static_cast<uint4*>(dst), row_map, sched, row_bytes / 16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, const float* zt,
+                           int n_tiles, long long stride, const int* pack_of, const uint8_t* mask,
+                           long long T, float* logprob, float* entropy, float* lse, int num_sms,
+                           cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  long long grid = (T + 255) / 256;
+  if (grid > 16LL * num_sms) grid = 16LL * num_sms;
+  combine_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(pm, ps, pu, zt, n_tiles, stride,
+                                                             pack_of, mask, T, logprob, entropy,
+                                                             lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T,
+                                      long long row_bytes, int num_sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const long long grid = T < 8LL * num_sms ? T : 8LL * num_sms;
+  zero_unpacked_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
+      static_cast<uint4*>(out), pack_of, T, row_bytes / 16);
+  return cudaGetLastError();
+}
+
+}  // namespace eas

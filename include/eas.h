@@ -1,0 +1,205 @@
+/*
+ * eas.h - C ABI of the GB300 (sm_103a) block-sparse fused LM-head.
+ *
+ * The operation is the one described on "perf(megatron): add block-sparse
+ * fused LM-head backward" (SkyRL PR #2376) and the layers it builds on
+ * (#2374 "fuse LM-head entropy for RL", #2375 "add block-sparse fused LM-head
+ * forward"):
+ *
+ *   - a loss mask marks which tokens (rows of `hidden`) are active;
+ *   - the mask is turned into ordered active spans, coalescing runs whose
+ *     inactive gap is at most max_gap (128 on the page, Bugbot "Overview");
+ *   - the forward returns, for every active token, the target-token log
+ *     probability and the softmax entropy of logits = hidden . W^T, computed
+ *     one vocabulary tile at a time with an online log-sum-exp, never
+ *     materialising the [T, V] logits;
+ *   - the backward builds d-logits only for active tiles ("What does this PR
+ *     do?", "How it works"), and projects them to dHidden and dW through the
+ *     ordered spans, one vocabulary chunk at a time, the final chunk sized to
+ *     its live width ("How it works"; greptile "Wide-tail grid exceeds live
+ *     split").
+ *
+ * Formulas (the page names them; these are their textbook definitions):
+ *   z      = W h_t                         W is [V, H] (nn.Linear layout)
+ *   lse_t  = log sum_v exp(z_v)
+ *   logp_t = z_target - lse_t
+ *   H_t    = lse_t - sum_v p_v z_v,        p = exp(z - lse_t)
+ *   dZ_t   = g_lp,t (onehot(target) - p) - g_H,t p (z - lse_t + H_t)
+ *   dHidden = dZ W,   dW = dZ^T hidden
+ * with g_lp = dL/dlogp and g_H = dL/dH (autograd convention: the gradient of
+ * L = sum_t g_lp,t logp_t + g_H,t H_t).  Rows whose mask byte is 0 have
+ * logp = H = lse = 0 and a zero dHidden row, whatever g holds there.
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, row-major,
+ *     16-byte aligned.  Nothing is allocated and the host is never
+ *     synchronised: every call only enqueues kernels on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream).
+ *   - Argument errors that the host can see are returned at once and nothing
+ *     is launched.  Errors only the device can see (spans that do not cover
+ *     the mask, a span buffer that is too small, a pipeline wait that ran out
+ *     of time) are written to a status word inside the workspace; read it with
+ *     eas_read_device_status().  The status word is cleared at the start of
+ *     every call that takes the workspace.
+ *   - eas_last_error() returns a thread-local message about the last error.
+ */
+#ifndef EAS_H_
+#define EAS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    EAS_OK = 0,
+    EAS_ERR_INVALID_ARG = 1,    /* a host-visible argument is wrong            */
+    EAS_ERR_INVALID_SPANS = 2,  /* spans unsorted, out of range, overlapping,
+                                   or an active token lies outside every span */
+    EAS_ERR_UNSUPPORTED = 3,    /* shape or alignment this build does not run  */
+    EAS_ERR_WORKSPACE = 4,      /* workspace missing or smaller than required */
+    EAS_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed           */
+    EAS_ERR_TIMEOUT = 6,        /* a kernel pipeline wait ran out of time      */
+    EAS_ERR_SPAN_CAPACITY = 7   /* more spans than the caller's buffer holds   */
+} eas_status;
+
+typedef enum {
+    EAS_BF16 = 0,   /* hidden, W, dhidden bf16; tensor cores, fp32 accumulate */
+    EAS_FP32 = 1    /* hidden, W, dhidden fp32; fp32 FMA throughout           */
+} eas_dtype;
+
+/* Row policy for the forward/backward (the `flags` argument). */
+#define EAS_ROWS_ACTIVE 0u  /* tensor-core work on the active rows of the
+                               spans only (gap rows inside a span skipped)   */
+#define EAS_ROWS_SPAN   1u  /* every row of every span, gap rows included
+                               (span-contiguous schedule; gap rows still get
+                               zero outputs and gradients)                  */
+
+/* Default vocabulary chunk width of the backward (columns of d-logits held
+ * in the staging buffer at once).  0 passed as vocab_chunk selects it. */
+#define EAS_DEFAULT_VOCAB_CHUNK 16384
+
+/* ------------------------------------------------------------------ spans */
+
+/* Bytes of workspace eas_build_active_spans needs for T tokens. */
+size_t eas_spans_workspace_size(int64_t T);
+
+/*
+ * Ordered active spans of a loss mask ("What does this PR do?": ordered
+ * active spans; Bugbot "Overview": coalesced with gaps <= 128).
+ *
+ *   mask      [T] uint8, nonzero = active token.
+ *   max_gap   >= 0; two maximal active runs merge into one span when the
+ *             number of inactive tokens between them is <= max_gap.
+ *   spans     [cap][2] int32, out: half-open [start, end) pairs, ascending;
+ *             spans start and end on active tokens.  Only the first
+ *             min(S, cap) pairs are written.
+ *   num_spans [1] int32 device, out: S, the true span count (may exceed cap,
+ *             in which case the status word reads EAS_ERR_SPAN_CAPACITY).
+ *   ws        workspace of eas_spans_workspace_size(T) bytes (holds the
+ *             status word).
+ * An empty mask gives S = 0; an all-active mask gives one span [0, T).
+ */
+eas_status eas_build_active_spans(const uint8_t* mask, int64_t T, int32_t max_gap,
+                                  int32_t* spans, int64_t cap, int32_t* num_spans,
+                                  void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------- LM head */
+
+/*
+ * Bytes of workspace eas_lmhead_fwd and eas_lmhead_bwd need (the larger of
+ * the two, so one workspace serves both).  vocab_chunk = 0 selects
+ * EAS_DEFAULT_VOCAB_CHUNK.
+ */
+size_t eas_lmhead_workspace_size(int64_t T, int64_t H, int64_t V, eas_dtype dtype,
+                                 int64_t vocab_chunk);
+
+/*
+ * Forward: target log-probability, softmax entropy and log-sum-exp of the
+ * active tokens (#2375 "add block-sparse fused LM-head forward", #2374 "fuse
+ * LM-head entropy for RL", as summarised on the #2376 page).
+ *
+ *   hidden   [T, H]  bf16 or fp32 (dtype)
+ *   weight   [V, H]  same dtype
+ *   targets  [T] int32, read only on active rows, must be in [0, V)
+ *   mask     [T] uint8 loss mask
+ *   spans, num_spans, cap : spans as produced by eas_build_active_spans (or
+ *            by the caller); they must be sorted, disjoint, inside [0, T)
+ *            and cover every active token, else the status word reads
+ *            EAS_ERR_INVALID_SPANS and all outputs are zero.
+ *   flags    EAS_ROWS_ACTIVE or EAS_ROWS_SPAN
+ *   logprob, entropy, lse  [T] fp32 out, overwritten; 0 on inactive rows.
+ * Requirements: H % 64 == 0 (bf16) or H % 4 == 0 (fp32); V >= 1; T >= 0.
+ */
+eas_status eas_lmhead_fwd(const void* hidden, const void* weight,
+                          const int32_t* targets, const uint8_t* mask,
+                          const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                          int64_t T, int64_t H, int64_t V, eas_dtype dtype, uint32_t flags,
+                          float* logprob, float* entropy, float* lse,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward: dHidden and dW of L = sum_active g_lp logp + g_H H ("What does
+ * this PR do?": skip inactive d-logits tiles, hidden-state gradients through
+ * ordered active spans; "How it works": final vocabulary split sized to its
+ * live width).
+ *
+ *   g_logprob, g_entropy [T] fp32 upstream gradients (ignored, even if NaN,
+ *            on inactive rows)
+ *   hidden, weight, targets, mask, spans, num_spans, cap, flags : as in the
+ *            forward (the same spans must be passed)
+ *   lse, entropy [T] fp32 : the forward's outputs for the same inputs
+ *   vocab_chunk : d-logits columns per chunk (0 = default); the last chunk
+ *            covers only the V - (n-1)*vocab_chunk live columns
+ *   dhidden  [T, H] out, hidden's dtype, overwritten; exactly 0 on rows whose
+ *            mask byte is 0
+ *   dweight  [V, H] fp32 out, overwritten (every row written)
+ */
+eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy,
+                          const void* hidden, const void* weight,
+                          const int32_t* targets, const uint8_t* mask,
+                          const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                          const float* lse, const float* entropy,
+                          int64_t T, int64_t H, int64_t V, eas_dtype dtype, uint32_t flags,
+                          int64_t vocab_chunk,
+                          void* dhidden, float* dweight,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------- utilities */
+
+/*
+ * Waits for `stream`, then returns the status word the device wrote into
+ * workspace `ws` during the last call that used it (EAS_OK if none).  This is
+ * the only entry point that synchronises the host.
+ */
+eas_status eas_read_device_status(const void* ws, void* stream);
+
+/*
+ * Per-kernel timing.  eas_trace_enable(1) clears earlier records and makes
+ * every later kernel launch of this library record a pair of CUDA events
+ * around itself on its stream; eas_trace_enable(0) stops recording.
+ * eas_trace_read() waits for the recorded events and writes, for the first
+ * min(n, cap) launches, the kernel kind (see eas_kernel_name) and its
+ * duration in milliseconds; it returns n, the number of recorded launches.
+ * For eager launches only (not inside a CUDA graph capture).
+ */
+void eas_trace_enable(int32_t on);
+int32_t eas_trace_read(int32_t* kinds, float* ms, int32_t cap);
+const char* eas_kernel_name(int32_t kind);
+
+/* Thread-local description of the last error returned on this thread. */
+const char* eas_last_error(void);
+
+/* Short name of a status code. */
+const char* eas_status_string(eas_status s);
+
+/* Version of this library: major * 10000 + minor * 100 + patch. */
+int32_t eas_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif  /* EAS_H_ */

@@ -11,3 +11,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: takes more than a few seconds")
+
+
+@pytest.fixture(scope="session")
+def libeas():
+    """The C-ABI library, built in-tree with nvcc if it is missing or stale."""
+    from entropy_active_span_gb300 import _lib, build
+    build.build()
+    return _lib.load()
