@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 block-sparse fused LM-head.
+
+One step = the whole hot path over one batch: active spans built on the device
+from the loss mask, the fused forward (target logprob, entropy, lse of the
+active tokens) and the backward (d-logits of active tiles, dHidden, dW), on
+the synthetic rl_16k workload by default (T=16384 tokens, H=4096, V=128256,
+bf16; 16 sequences of 1024 tokens whose first 256..512 prompt tokens are
+inactive).  Metric: active tokens per second of fwd+bwd, and the fraction of
+the GB300 dense-bf16 tensor peak achieved on active FLOPs (8 * Ta * H * V per
+step: forward logits, backward recompute, dHidden and dW, each 2 * Ta * H * V).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload rl_16k] [--max-gap 128] [--vocab-chunk 0]
+
+Prints one JSON line on rank 0.  --impl reference times the CPU oracle (fp64
+NumPy) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from entropy_active_span_gb300 import workloads as W  # noqa: E402
+
+METRIC = "active tokens/sec fwd+bwd; % of GB300 bf16 tensor peak on active FLOPs"
+UNIT = "active tokens/s"
+GEMM_KINDS = ("fwd_gemm_tc", "dlogits_gemm_tc", "dhidden_gemm_tc", "dweight_gemm_tc")
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=40)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="rl_16k", choices=sorted(W.ALL_WORKLOADS))
+    p.add_argument("--max-gap", type=int, default=128)
+    p.add_argument("--vocab-chunk", type=int, default=0)
+    p.add_argument("--rows", choices=("active", "span"), default="active")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-dense", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(bf16=d["bf16_tflops"], bf16_sustained=d["bf16_tflops_sustained"],
+                    hbm=d["hbm_gbs"], source="measured")
+    return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rate(inp, target_s: float):
+    """Times the fp64 oracle's fwd+bwd on a sample of active rows (rows/s)."""
+    import oracle
+    act = np.flatnonzero(inp["mask"])
+    Wf = W.to_f64(inp["weight"])
+    rng = np.random.default_rng(0)
+
+    def run(n):
+        rows = np.sort(rng.choice(act, size=min(n, len(act)), replace=False))
+        h = W.to_f64(inp["hidden"][rows])
+        t0 = time.perf_counter()
+        oracle.lmhead_forward_rows(h, Wf, inp["targets"][rows])
+        oracle.lmhead_backward_rows_weighted(h, Wf, inp["targets"][rows],
+                                             inp["g_logprob"][rows], inp["g_entropy"][rows])
+        return len(rows), time.perf_counter() - t0
+
+    n0, t0 = run(8)
+    per_row = t0 / max(n0, 1)
+    n = int(max(8, min(len(act), target_s / max(per_row, 1e-9))))
+    n, t = run(n)
+    return n, t
+
+
+def reference_arm(args, rank):
+    """--impl reference: the CPU oracle as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = W.ALL_WORKLOADS[args.workload]
+    inp = W.make_inputs(w)
+    import oracle
+    act = np.flatnonzero(inp["mask"])
+    Wf = W.to_f64(inp["weight"])
+    rng = np.random.default_rng(1)
+    # size the per-step sample so one step is about args.cpu_seconds / 2
+    h8 = W.to_f64(inp["hidden"][act[:8]])
+    t0 = time.perf_counter()
+    oracle.lmhead_forward_rows(h8, Wf, inp["targets"][act[:8]])
+    oracle.lmhead_backward_rows_weighted(h8, Wf, inp["targets"][act[:8]],
+                                         inp["g_logprob"][act[:8]], inp["g_entropy"][act[:8]])
+    per_row = (time.perf_counter() - t0) / 8
+    n = int(max(8, min(len(act), 0.5 * args.cpu_seconds / max(per_row, 1e-9))))
+    times = []
+    for i in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(act, size=n, replace=False))
+        h = W.to_f64(inp["hidden"][rows])
+        t0 = time.perf_counter()
+        oracle.lmhead_forward_rows(h, Wf, inp["targets"][rows])
+        oracle.lmhead_backward_rows_weighted(h, Wf, inp["targets"][rows],
+                                             inp["g_logprob"][rows], inp["g_entropy"][rows])
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = n * len(times) / total
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "T": w.T, "H": w.H, "V": w.V,
+                   "active_tokens": int(len(act)), "max_gap": args.max_gap},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} random active rows per step at full H={w.H}, V={w.V}: "
+                                   "fp64 forward + d-logits + dHidden + dW contribution"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                   "-lms", "200"]
+            if uuid:
+                cmd += ["-i", uuid]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# -------------------------------------------------------------- our arm
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import entropy_active_span_gb300 as eas
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl")
+
+    w = W.ALL_WORKLOADS[args.workload]
+    if w.dtype != "bf16":
+        raise SystemExit("bench measures the bf16 tensor-core path")
+    wr = w.replace(seed=w.seed + 1000 * rank)     # each rank: its own batch (weak scaling)
+    inp = W.make_inputs(wr)
+    T, H, V = w.T, w.H, w.V
+    Ta = int(inp["mask"].sum())
+    flags = eas.EAS_ROWS_SPAN if args.rows == "span" else eas.EAS_ROWS_ACTIVE
+
+    def d(x):
+        t = torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        return t.view(torch.bfloat16) if x.dtype == np.uint16 else t
+
+    hidden, weight = d(inp["hidden"]), d(inp["weight"])
+    targets, mask = d(inp["targets"]), d(inp["mask"])
+    glp, gh = d(inp["g_logprob"]), d(inp["g_entropy"])
+    cap = (T + 1) // 2
+    spans = torch.empty((cap, 2), dtype=torch.int32, device=dev)
+    ns = torch.empty(1, dtype=torch.int32, device=dev)
+    sws = eas.workspace(eas.spans_workspace_size(T), dev)
+    ws = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.bfloat16, args.vocab_chunk), dev)
+    lp, ent, lse = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
+    dh = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((V, H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(m=mask):
+        eas.build_active_spans(m, args.max_gap, spans=spans, num_spans=ns, ws=sws)
+        eas.lmhead_fwd(hidden, weight, targets, m, spans, ns, flags, ws=ws, out=(lp, ent, lse))
+        eas.lmhead_bwd(glp, gh, hidden, weight, targets, m, spans, ns, lse, ent, flags,
+                       args.vocab_chunk, ws=ws, dhidden=dh, dweight=dw)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def timed(fn, k, trace=False):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if trace:
+            eas.trace_enable(True)
+        e0.record(stream)
+        for _ in range(k):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        recs = None
+        if trace:
+            eas.trace_enable(False)
+            recs = eas.trace_read()
+        barrier()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms / k, recs
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
+
+    # ---- main timed region (device-resident inputs)
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    ms, recs = timed(step, args.steps, trace=True)
+    clocks = sampler.stop() if sampler else None
+    assert eas.read_device_status(ws) == 0 and eas.read_device_status(sws) == 0
+
+    tot_tokens = torch.tensor([float(Ta)], device=dev)
+    if world > 1:
+        dist.all_reduce(tot_tokens)
+    tokens_all = float(tot_tokens.item())
+    value = tokens_all / (ms / 1000.0)
+    pk = peaks()
+    flops_step = 8.0 * Ta * H * V
+    tflops = flops_step / (ms / 1000.0) / 1e12
+
+    # per-kernel breakdown from the library's event trace
+    by = {}
+    for name, t in recs:
+        e = by.setdefault(name, [0, 0.0])
+        e[0] += 1
+        e[1] += t
+    launches = sum(c for n, (c, _) in by.items() if n != "memset")
+    gemm = {k: v for k, v in by.items() if k in GEMM_KINDS}
+    top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
+    roofline = None
+    if top is not None:
+        name, (count, tot_ms) = top
+        flops_kind = 2.0 * Ta * H * V * args.steps       # each GEMM kind: 2 Ta H V per step
+        achieved = flops_kind / (tot_ms / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "kernel": name, "achieved": achieved,
+                    "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                    "frac": achieved / pk["bf16_sustained"], "traffic": None,
+                    "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+                    "launches_per_step": count / args.steps,
+                    "ms_per_launch": tot_ms / count}
+    kernels = {k: round(v[1] / args.steps, 4) for k, v in sorted(by.items())}
+
+    # ---- dense-mask ablation (same kernels, every token active)
+    dense = None
+    if not args.no_dense:
+        ones = torch.ones(T, dtype=torch.uint8, device=dev)
+        dms, _ = timed(lambda: step(ones), args.steps)
+        dense = {"ms_per_step": dms, "active_tokens_per_s": world * T / (dms / 1000.0),
+                 "tflops": 8.0 * T * H * V / (dms / 1000.0) / 1e12,
+                 "frac_of_peak": 8.0 * T * H * V / (dms / 1000.0) / 1e12 / pk["bf16_sustained"]}
+
+    # ---- end to end: host (pinned) inputs in, results out, through the API
+    e2e = None
+    if not args.no_e2e:
+        host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory()
+                for k in ("hidden", "weight", "targets", "mask", "g_logprob", "g_entropy")}
+        dev_in = {"hidden": hidden, "weight": weight, "targets": targets, "mask": mask,
+                  "g_logprob": glp, "g_entropy": gh}
+        out_lp = torch.empty(T, dtype=torch.float32).pin_memory()
+        out_ent = torch.empty(T, dtype=torch.float32).pin_memory()
+
+        def e2e_step():
+            for k, hsrc in host.items():
+                dst = dev_in[k]
+                dst.view(torch.uint8).view(-1).copy_(hsrc.view(torch.uint8).view(-1),
+                                                     non_blocking=True)
+            step()
+            out_lp.copy_(lp, non_blocking=True)
+            out_ent.copy_(ent, non_blocking=True)
+
+        ems, _ = timed(e2e_step, args.steps)
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = 2 * T * 4
+        e2e = {"value": tokens_all / (ems / 1000.0), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+               "note": "H2D of hidden, W, targets, mask, g_logprob, g_entropy from pinned host "
+                       "memory; D2H of logprob and entropy; gradients stay on the device"}
+
+    # ---- CPU oracle baseline (rank 0, N=1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, t = oracle_sample_rate(inp, args.cpu_seconds)
+        cpu = {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
+               "sample": f"{n} random active rows at full H={H}, V={V}: fp64 forward + "
+                         f"d-logits + dHidden + dW contribution, {t:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "T": T, "H": H, "V": V,
+                       "active_tokens_per_rank": Ta, "max_gap": args.max_gap,
+                       "rows": args.rows, "vocab_chunk": args.vocab_chunk or 16384,
+                       "parallelism": f"replicas x{world} (independent batches)",
+                       "l2": "inputs larger than L2 (W alone is %.2f GB)" % (V * H * 2 / 1e9)},
+            "tflops_active": tflops,
+            "frac_of_peak": tflops / pk["bf16_sustained"],
+            "peak_tflops": pk["bf16_sustained"],
+            "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+            "roofline": roofline,
+            "kernels_ms_per_step": kernels,
+            "gpu_launches": launches,
+            "dense_ablation": dense,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -66,6 +66,15 @@ WORKLOADS = {
                     "prompt 2458..4096 inactive"),
 }
 
+# A reduced shape of the RL workload for profiler captures (W still larger
+# than L2, about 1 GB on the device in total).
+PROFILE_WORKLOADS = {
+    "rl_4k_v32k": Workload(
+        "rl_4k_v32k", 4096, 4096, 32768, "bf16", 1102, "rl_prompts_1024",
+        description="T=4096 H=4096 V=32768 bf16; 4 sequences x 1024, prompt 256..512 inactive"),
+}
+ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
+
 
 def _streams(seed: int):
     names = ("mask", "targets", "hidden", "weight", "g_logprob", "g_entropy")
@@ -251,7 +260,7 @@ def make_inputs(w: Workload | str, *, mask_kind: str | None = None,
     ``mask_kind`` swaps the mask (e.g. "dense" for the all-active ablation);
     ``w_std`` swaps the std of W (to give peaked, far-from-uniform softmaxes)."""
     if isinstance(w, str):
-        w = WORKLOADS[w]
+        w = ALL_WORKLOADS[w]
     if mask_kind is not None:
         w = w.replace(mask_kind=mask_kind)
     g_lp, g_h = make_upstream(w)

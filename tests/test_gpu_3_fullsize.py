@@ -1,0 +1,99 @@
+"""GPU parity at the five workloads' full sizes, in the launch configuration
+bench.py times (spans with max_gap 128, active-row schedule, default vocab
+chunk).
+
+The oracle cannot afford whole problems here, so:
+  * logprob / entropy / lse and dHidden are row-local: sampled rows (first and
+    last active token of spread-out spans, rows at 128-row tile boundaries of
+    the packed order, random active rows) are compared one by one;
+  * every inactive row is checked to be exactly zero on the whole output;
+  * dW couples all rows, so a second backward uses upstream gradients that
+    vanish outside a row sample S: dW is then exactly sum_{r in S} dZ_r^T h_r,
+    which the oracle computes, and the whole [V, H] matrix is compared.
+"""
+import numpy as np
+import pytest
+import torch
+
+import entropy_active_span_gb300 as eas
+from entropy_active_span_gb300 import workloads as W
+from gpu_helpers import BF16_TOL, FP32_TOL, rel_fro, to_dev
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def sample_rows(mask, spans, rng, n_random=48):
+    act = np.flatnonzero(mask)
+    picks = set()
+    if len(spans):
+        for k in np.unique(np.linspace(0, len(spans) - 1, min(12, len(spans))).astype(int)):
+            s, e = spans[k]
+            a = act[(act >= s) & (act < e)]
+            picks.update((int(a[0]), int(a[-1])))
+    step = max(128, (len(act) // (12 * 128)) * 128)
+    for p in range(0, len(act), step):
+        picks.add(int(act[p]))
+        picks.add(int(act[min(p + 127, len(act) - 1)]))
+    picks.update(int(x) for x in rng.choice(act, size=min(n_random, len(act)), replace=False))
+    picks.add(int(act[-1]))
+    return np.array(sorted(picks), np.int64)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "rl_16k", "packed_64k", "sparse_128k", "long_256k"])
+def test_full_size_workload(name):
+    w = W.WORKLOADS[name]
+    inp = W.make_inputs(w)
+    tol = FP32_TOL if w.dtype == "fp32" else BF16_TOL
+    T, H, V = w.T, w.H, w.V
+    mask_np = inp["mask"]
+    hidden, weight = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    targets, mask = to_dev(inp["targets"]), to_dev(mask_np)
+    glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
+    spans, ns = eas.build_active_spans(mask, 128)
+    ws = eas.workspace(eas.lmhead_workspace_size(T, H, V, hidden.dtype), hidden.device)
+    lp, ent, lse = eas.lmhead_fwd(hidden, weight, targets, mask, spans, ns, ws=ws)
+    assert eas.read_device_status(ws) == 0
+    dh, dw = eas.lmhead_bwd(glp, gh, hidden, weight, targets, mask, spans, ns, lse, ent, ws=ws)
+    assert eas.read_device_status(ws) == 0
+    n = int(ns.item())
+    spans_np = spans[:n].cpu().numpy().astype(np.int64)
+    np.testing.assert_array_equal(spans_np, oracle.active_spans(mask_np, 128))
+
+    inactive = torch.from_numpy(mask_np == 0).cuda()
+    for t in (lp, ent, lse):
+        assert torch.all(t[inactive] == 0)
+    assert torch.all(dh[inactive] == 0)
+
+    rng = np.random.default_rng(w.seed)
+    rows = sample_rows(mask_np, spans_np, rng)
+    W64 = W.to_f64(inp["weight"])
+    h_rows = W.to_f64(inp["hidden"][rows])
+    rlp, rent, rlse = oracle.lmhead_forward_rows(h_rows, W64, inp["targets"][rows])
+    ridx = torch.from_numpy(rows).cuda()
+    assert np.max(np.abs(lp[ridx].cpu().numpy() - rlp)) <= tol["lp"]
+    assert np.max(np.abs(ent[ridx].cpu().numpy() - rent)) <= tol["ent"]
+    assert np.max(np.abs(lse[ridx].cpu().numpy() - rlse)) <= tol["lp"]
+    dz = oracle.lmhead_dlogits_rows(h_rows, W64, inp["targets"][rows],
+                                    inp["g_logprob"][rows], inp["g_entropy"][rows])
+    assert rel_fro(dh[ridx].float().cpu().numpy(), dz @ W64) <= tol["fro"]
+    del dz
+
+    # dW at full size: upstream gradients vanish outside the row sample S
+    S = rows[:: max(1, len(rows) // 64)]
+    g1 = np.zeros(T, np.float32)
+    g2 = np.zeros(T, np.float32)
+    g1[S] = inp["g_logprob"][S]
+    g2[S] = inp["g_entropy"][S]
+    dh2, dw2 = eas.lmhead_bwd(to_dev(g1), to_dev(g2), hidden, weight, targets, mask, spans, ns,
+                              lse, ent, ws=ws)
+    assert eas.read_device_status(ws) == 0
+    rdh, rdw = oracle.lmhead_backward_rows_weighted(W.to_f64(inp["hidden"][S]), W64,
+                                                    inp["targets"][S], g1[S], g2[S])
+    assert rel_fro(dw2.cpu().numpy(), rdw) <= tol["fro"]
+    sidx = torch.from_numpy(S).cuda()
+    assert rel_fro(dh2[sidx].float().cpu().numpy(), rdh) <= tol["fro"]
+    # rows outside S now have zero upstream gradient, hence a zero dHidden row
+    others = torch.ones(T, dtype=torch.bool, device="cuda")
+    others[sidx] = False
+    assert torch.all(dh2[others] == 0)
