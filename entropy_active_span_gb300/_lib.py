@@ -23,6 +23,7 @@ EAS_ROWS_ACTIVE = 0
 EAS_ROWS_SPAN = 1
 
 EAS_DEFAULT_VOCAB_CHUNK = 16384
+EAS_STATIC_SCRATCH_BYTES = 64 << 20
 
 # name -> (restype, argtypes), in the order of include/eas.h
 _P, _I64, _I32, _U32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
@@ -35,6 +36,8 @@ SIGNATURES = {
     "eas_lmhead_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P,
                                       _I64, _I64, _I64, ctypes.c_int, _U32, _I64,
                                       _P, _P, _P, _SZ, _P]),
+    "eas_lmhead_fwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                              ctypes.c_int, _U32, _P, _P, _P, _P]),
     "eas_read_device_status": (ctypes.c_int, [_P, _P]),
     "eas_trace_enable": (None, [_I32]),
     "eas_trace_read": (ctypes.c_int32, [_P, _P, _I32]),

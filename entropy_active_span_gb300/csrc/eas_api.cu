@@ -667,3 +667,16 @@ const char* eas_status_string(eas_status s) {
 int32_t eas_version(void) { return 100; }
 
 }  // extern "C"
+
+namespace eas {
+
+// Forward-only workspace requirement (the larger backward part excluded).
+size_t lmhead_fwd_workspace_bytes(long long T, long long H, long long V, int dtype) {
+  if (T < 0 || H < 1 || V < 1) return 0;
+  return layout(T, H, V, static_cast<eas_dtype>(dtype), 0).fwd_end;
+}
+
+// Replaces this thread's eas_last_error() message.
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
+}  // namespace eas

@@ -119,3 +119,9 @@ struct SimtArgs {
 cudaError_t launch_simt_gemm(const SimtArgs& args, long long max_tiles, cudaStream_t s);
 
 }  // namespace eas
+
+namespace eas {
+// ---- helpers the C-ABI translation units share (eas_api.cu) ----
+size_t lmhead_fwd_workspace_bytes(long long T, long long H, long long V, int dtype);
+void set_last_error(const char* msg);
+}  // namespace eas

@@ -167,6 +167,46 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy,
                           void* dhidden, float* dweight,
                           void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------- allocation-free forward */
+
+/*
+ * eas_lmhead_fwd without a workspace argument.  This entry point has no
+ * counterpart on the page; it exists for callers that cannot allocate device
+ * memory when they run the forward: a host whose pool allocator owns all of
+ * the GPU's memory and lends none to libraries, an embedded or real-time host
+ * that forbids allocation after start-up, or a plugin interface that hands a
+ * library only its input and output buffers.
+ *
+ * Its scratch is a static device array of EAS_STATIC_SCRATCH_BYTES (64 MiB)
+ * compiled into the library; every GPU that loads the library reserves it
+ * until the process exits.  Arguments, outputs and results are those of
+ * eas_lmhead_fwd; the caller still passes every input and output buffer.
+ *   - Problems whose forward needs more scratch than that are rejected with
+ *     EAS_ERR_WORKSPACE before anything is launched, and eas_last_error()
+ *     gives the bytes needed (eas_lmhead_fwd with a workspace has no limit).
+ *     For bf16 the need is about T * (2H + 12 ceil(V/256) + 16) bytes.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with that device current); make that first
+ *     call before any stream capture.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call
+ *     (leave eas_trace_enable off, since tracing creates CUDA events).
+ *   - All calls share the one array, and it keeps what the last call left
+ *     there; each call clears what must start at zero.  Calls whose kernels
+ *     overlap on the GPU (different streams, or different host threads
+ *     without ordering) race on the array and give wrong results: order them.
+ *   - The device status word lives in the shared array and cannot be read
+ *     back through this entry point; as with eas_lmhead_fwd, spans that fail
+ *     validation leave every output zero.
+ */
+#define EAS_STATIC_SCRATCH_BYTES (64ull << 20)
+
+eas_status eas_lmhead_fwd_noalloc(const void* hidden, const void* weight,
+                                  const int32_t* targets, const uint8_t* mask,
+                                  const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                                  int64_t T, int64_t H, int64_t V, eas_dtype dtype,
+                                  uint32_t flags, float* logprob, float* entropy, float* lse,
+                                  void* stream);
+
 /* ------------------------------------------------------------- utilities */
 
 /*
