@@ -36,7 +36,29 @@ from entropy_active_span_gb300 import workloads as W  # noqa: E402
 
 METRIC = "active tokens/sec fwd+bwd; % of GB300 bf16 tensor peak on active FLOPs"
 UNIT = "active tokens/s"
-GEMM_KINDS = ("fwd_gemm_tc", "dlogits_gemm_tc", "dhidden_gemm_tc", "dweight_gemm_tc")
+GEMM_KINDS = ("fwd_gemm_tc", "dlogits_gemm_tc", "bwd_chunk_gemm_tc", "dproj_gemm_tc")
+
+
+def kind_flops(name: str, Ta: int, H: int, V: int, chunk: int) -> float:
+    """Algorithmic FLOPs per step of each traced tensor-core launch kind.
+
+    Every contraction is 2 * Ta * H * (vocabulary columns it covers).  The
+    backward runs d-logits of chunk 0 alone, then launches that hold dW and
+    dHidden of chunk c-1 with the d-logits of chunk c, then dW and dHidden of
+    the last chunk."""
+    vc = min(chunk, V)
+    n = -(-V // vc)
+    live = [min(vc, V - c * vc) for c in range(n)]
+    u = 2.0 * Ta * H
+    if name == "fwd_gemm_tc":
+        return u * V
+    if name == "dlogits_gemm_tc":
+        return u * live[0]
+    if name == "bwd_chunk_gemm_tc":
+        return u * sum(2 * live[c - 1] + live[c] for c in range(1, n))
+    if name == "dproj_gemm_tc":
+        return u * 2 * live[-1]
+    return 0.0
 
 
 def parse_args():
@@ -313,7 +335,7 @@ def main():
     roofline = None
     if top is not None:
         name, (count, tot_ms) = top
-        flops_kind = 2.0 * Ta * H * V * args.steps       # each GEMM kind: 2 Ta H V per step
+        flops_kind = kind_flops(name, Ta, H, V, args.vocab_chunk or 16384) * args.steps
         achieved = flops_kind / (tot_ms / 1000.0) / 1e12
         roofline = {"bound": "tensor", "kernel": name, "achieved": achieved,
                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
@@ -322,6 +344,8 @@ def main():
                     "launches_per_step": count / args.steps,
                     "ms_per_launch": tot_ms / count}
     kernels = {k: round(v[1] / args.steps, 4) for k, v in sorted(by.items())}
+    gemm_tflops = {k: round(kind_flops(k, Ta, H, V, args.vocab_chunk or 16384) * args.steps
+                            / (v[1] / 1000.0) / 1e12, 1) for k, v in gemm.items()}
 
     # ---- dense-mask ablation (same kernels, every token active)
     dense = None
@@ -384,6 +408,7 @@ def main():
             "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
             "roofline": roofline,
             "kernels_ms_per_step": kernels,
+            "gemm_tflops": gemm_tflops,
             "gpu_launches": launches,
             "dense_ablation": dense,
             "e2e": e2e,

@@ -90,18 +90,22 @@ long long wait_budget() {
 // When enabled, every kernel launch of the library is bracketed by a pair of
 // CUDA events on its stream, tagged with the kernel's kind; eas_trace_read()
 // returns the durations.  Off by default; meant for eager (not captured)
-// launches.
+// launches.  Backward tensor-core launches are named by their jobs:
+// dlogits_gemm_tc (d-logits of chunk 0), bwd_chunk_gemm_tc (dW and dHidden of
+// chunk c-1 with the d-logits of chunk c), dproj_gemm_tc (dW and dHidden of
+// the last chunk).
 
 enum TraceKind : int {
   kTrSpans = 0, kTrRowmap, kTrGather, kTrFwdGemm, kTrCombine, kTrZeroRows,
-  kTrDLogitsGemm, kTrDHiddenGemm, kTrDWeightGemm, kTrSimtFwd, kTrSimtDLogits,
-  kTrSimtDHidden, kTrSimtDWeight, kTrMemset, kTrCount
+  kTrDLogitsGemm, kTrDProjGemm, kTrUnused, kTrSimtFwd, kTrSimtDLogits,
+  kTrSimtDHidden, kTrSimtDWeight, kTrMemset, kTrBwdChunkGemm, kTrCount
 };
 
 const char* const kTraceNames[kTrCount] = {
     "spans_build", "rowmap", "gather_rows", "fwd_gemm_tc", "combine", "zero_rows",
-    "dlogits_gemm_tc", "dhidden_gemm_tc", "dweight_gemm_tc", "fwd_gemm_simt",
-    "dlogits_gemm_simt", "dhidden_gemm_simt", "dweight_gemm_simt", "memset"};
+    "dlogits_gemm_tc", "dproj_gemm_tc", "unused", "fwd_gemm_simt",
+    "dlogits_gemm_simt", "dhidden_gemm_simt", "dweight_gemm_simt", "memset",
+    "bwd_chunk_gemm_tc"};
 
 struct TraceRec {
   int kind;
@@ -188,9 +192,10 @@ struct Layout {
   long long vc;        // vocabulary chunk of the backward
   int n_chunks;
   long long ldz;       // staging row pitch (elements)
-  size_t status, sched, row_map, pack_of, hp;   // common part
+  size_t status, sched, counters, head_end;      // cleared at the start of each call
+  size_t row_map, pack_of, hp;                   // common part
   size_t pm, ps, pu, zt;                          // forward part
-  size_t dz, acc;                                 // backward part
+  size_t dz, dz2, acc;                            // backward part (two staging buffers)
   size_t fwd_end, bwd_end, total;
 };
 
@@ -209,6 +214,8 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   size_t o = 0;
   L.status = o; o = align_up(o + sizeof(DevStatus));
   L.sched = o; o = align_up(o + sizeof(Sched));
+  L.counters = o; o = align_up(o + sizeof(int) * static_cast<size_t>(L.n_chunks + 2));
+  L.head_end = o;
   L.row_map = o; o = align_up(o + 4 * static_cast<size_t>(L.T_pad > 0 ? L.T_pad : 1));
   L.pack_of = o; o = align_up(o + 4 * static_cast<size_t>(T > 0 ? T : 1));
   L.hp = o; o = align_up(o + esz * static_cast<size_t>(L.T_pad) * H);
@@ -220,6 +227,8 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   L.fwd_end = o;
   o = common;
   L.dz = o; o = align_up(o + esz * static_cast<size_t>(L.T_pad) * L.ldz);
+  L.dz2 = o;
+  if (dt == EAS_BF16 && L.n_chunks > 1) o = align_up(o + esz * static_cast<size_t>(L.T_pad) * L.ldz);
   L.acc = o;
   if (L.n_chunks > 1) o = align_up(o + 4 * static_cast<size_t>(L.T_pad) * H);
   L.bwd_end = o;
@@ -252,7 +261,7 @@ eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* span
                     cudaStream_t s) {
   {
     Trace tr_(kTrMemset, s);
-    EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, 2 * 1024, s), "clear status");
+    EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.status), 0, L.head_end, s), "clear status");
   }
   if (T == 0) return EAS_OK;
   {
@@ -355,19 +364,21 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
   if (dtype == EAS_BF16) {
     TcArgs a;
     memset(&a, 0, sizeof(a));
-    st = make_map_bf16(&a.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128);
+    TcJob& j = a.jobs[0];
+    st = make_map_bf16(&j.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128);
     if (st != EAS_OK) return st;
-    st = make_map_bf16(&a.tmB, weight, H, V, H, 256);
+    st = make_map_bf16(&j.tmB, weight, H, V, H, 256);
     if (st != EAS_OK) return st;
+    j.kind = kTcFwd;
+    j.M_fixed = 0;
+    j.N = static_cast<int>(V);
+    j.K_fixed = static_cast<int>(H);
+    j.group_m = group_for(128LL * H * 2, num_m_max);
+    a.n_jobs = 1;
     a.sched = sched;
     a.status = at<DevStatus>(ws, L.status);
+    a.tile_counter = at<int>(ws, L.counters);
     a.budget = wait_budget();
-    a.kind = kTcFwd;
-    a.M_fixed = 0;
-    a.N = static_cast<int>(V);
-    a.K_fixed = static_cast<int>(H);
-    a.group_m = group_for(128LL * H * 2, num_m_max);
-    a.v0 = 0;
     a.row_map = at<int>(ws, L.row_map);
     a.targets = targets;
     a.part_m = at<float>(ws, L.pm);
@@ -461,6 +472,10 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
   const long long num_m_max = L.T_pad / 128;
 
   if (dtype == EAS_BF16) {
+    // Launch c (0..n) runs dW and dHidden of chunk c-1 (reading staging
+    // buffer (c-1)%2) next to the d-logits of chunk c (writing buffer c%2):
+    // the jobs of one launch are independent and share the machine, and each
+    // launch boundary orders a chunk's d-logits before its projections.
     CUtensorMap hp_k, w_k, w_mn, hp_mn;
     if ((st = make_map_bf16(&hp_k, at<char>(ws, L.hp), H, L.T_pad, H, 128)) != EAS_OK) return st;
     if ((st = make_map_bf16(&w_k, weight, H, V, H, 256)) != EAS_OK) return st;
@@ -480,63 +495,72 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
     base.g_h = g_entropy;
     base.V = static_cast<int>(V);
     base.H = static_cast<int>(H);
-    base.dz = at<char>(ws, L.dz);
     base.ldz = L.ldz;
     base.acc = at<float>(ws, L.acc);
     base.dhidden = dhidden;
     base.dW = dweight;
-    for (int c = 0; c < L.n_chunks; ++c) {
-      const long long v0 = c * L.vc;
-      const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
-      // d-logits of the active rows, this chunk's live columns only
+    void* staging[2] = {at<char>(ws, L.dz), at<char>(ws, L.n_chunks > 1 ? L.dz2 : L.dz)};
+    for (int c = 0; c <= L.n_chunks; ++c) {
       TcArgs a = base;
-      a.tmA = hp_k;
-      a.tmB = w_k;
-      a.kind = kTcDLogits;
-      a.M_fixed = 0;
-      a.N = static_cast<int>(live);
-      a.K_fixed = static_cast<int>(H);
-      a.group_m = group_for(128LL * H * 2, num_m_max);
-      a.v0 = static_cast<int>(v0);
-      a.vc_live = static_cast<int>(live);
-      {
-        Trace tr_(kTrDLogitsGemm, s);
-        EAS_CUDA(launch_tc_gemm(a, grid_for(num_m_max * cdiv(live, kTcBN), di.sms), s), "dlogits");
+      a.tile_counter = at<int>(ws, L.counters) + c;
+      long long tiles = 0;
+      int trace_kind = kTrDLogitsGemm;
+      // projections of the previous chunk: dW (longest tiles when R is
+      // large) and dHidden first, the short d-logits tiles last
+      if (c > 0) {
+        const int p = c - 1;
+        const long long v0 = p * L.vc;
+        const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
+        void* dz = staging[p % 2];
+        CUtensorMap dz_k, dz_mn;
+        if ((st = make_map_bf16(&dz_k, dz, live, L.T_pad, L.ldz, 128)) != EAS_OK) return st;
+        if ((st = make_map_bf16(&dz_mn, dz, live, L.T_pad, L.ldz, 64)) != EAS_OK) return st;
+        TcJob& w = a.jobs[a.n_jobs++];
+        w.tmA = dz_mn;
+        w.tmB = hp_mn;
+        w.kind = kTcDWeight;
+        w.M_fixed = static_cast<int>(live);
+        w.N = static_cast<int>(H);
+        w.K_fixed = 0;
+        w.group_m = group_for(128LL * L.T_pad * 2, cdiv(live, kTcBM));
+        w.v0 = static_cast<int>(v0);
+        w.vc_live = static_cast<int>(live);
+        tiles += cdiv(live, kTcBM) * cdiv(H, kTcBN);
+        TcJob& h = a.jobs[a.n_jobs++];
+        h.tmA = dz_k;
+        h.tmB = w_mn;
+        h.kind = kTcDHidden;
+        h.M_fixed = 0;
+        h.N = static_cast<int>(H);
+        h.K_fixed = static_cast<int>(live);
+        h.group_m = group_for(128LL * live * 2, num_m_max);
+        h.v0 = static_cast<int>(v0);
+        h.vc_live = static_cast<int>(live);
+        h.first_chunk = (p == 0);
+        h.last_chunk = (p == L.n_chunks - 1);
+        tiles += num_m_max * cdiv(H, kTcBN);
+        trace_kind = kTrDProjGemm;
       }
-      CUtensorMap dz_k, dz_mn;
-      if ((st = make_map_bf16(&dz_k, base.dz, live, L.T_pad, L.ldz, 128)) != EAS_OK) return st;
-      if ((st = make_map_bf16(&dz_mn, base.dz, live, L.T_pad, L.ldz, 64)) != EAS_OK) return st;
-      // dHidden of the packed rows
-      TcArgs h = base;
-      h.tmA = dz_k;
-      h.tmB = w_mn;
-      h.kind = kTcDHidden;
-      h.M_fixed = 0;
-      h.N = static_cast<int>(H);
-      h.K_fixed = static_cast<int>(live);
-      h.group_m = group_for(128LL * live * 2, num_m_max);
-      h.v0 = static_cast<int>(v0);
-      h.vc_live = static_cast<int>(live);
-      h.first_chunk = (c == 0);
-      h.last_chunk = (c == L.n_chunks - 1);
-      {
-        Trace tr_(kTrDHiddenGemm, s);
-        EAS_CUDA(launch_tc_gemm(h, grid_for(num_m_max * cdiv(H, kTcBN), di.sms), s), "dhidden");
+      if (c < L.n_chunks) {
+        const long long v0 = c * L.vc;
+        const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
+        TcJob& d = a.jobs[a.n_jobs++];
+        d.tmA = hp_k;
+        d.tmB = w_k;
+        d.kind = kTcDLogits;
+        d.M_fixed = 0;
+        d.N = static_cast<int>(live);
+        d.K_fixed = static_cast<int>(H);
+        d.group_m = group_for(128LL * H * 2, num_m_max);
+        d.v0 = static_cast<int>(v0);
+        d.vc_live = static_cast<int>(live);
+        d.dz = staging[c % 2];
+        tiles += num_m_max * cdiv(live, kTcBN);
+        if (c > 0) trace_kind = kTrBwdChunkGemm;
       }
-      // dW rows of this chunk
-      TcArgs w = base;
-      w.tmA = dz_mn;
-      w.tmB = hp_mn;
-      w.kind = kTcDWeight;
-      w.M_fixed = static_cast<int>(live);
-      w.N = static_cast<int>(H);
-      w.K_fixed = 0;
-      w.group_m = group_for(128LL * L.T_pad * 2, cdiv(live, kTcBM));
-      w.v0 = static_cast<int>(v0);
-      w.vc_live = static_cast<int>(live);
       {
-        Trace tr_(kTrDWeightGemm, s);
-        EAS_CUDA(launch_tc_gemm(w, grid_for(cdiv(live, kTcBM) * cdiv(H, kTcBN), di.sms), s), "dweight");
+        Trace tr_(trace_kind, s);
+        EAS_CUDA(launch_tc_gemm(a, grid_for(tiles, di.sms), s), "backward gemm");
       }
     }
   } else {

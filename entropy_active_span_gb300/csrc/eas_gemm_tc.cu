@@ -12,17 +12,23 @@
 //   kTcDWeight  dZ_c^T      MN-major      Hp [R, H]   MN-major    dW rows (fp32)
 //
 // Hp is the row-packed copy of hidden (rows of the ordered spans), so every M
-// tile is dense; the grid is sized from live extents only (greptile "Wide-tail
+// tile is dense; tile counts come from live extents only (greptile "Wide-tail
 // grid exceeds live split": programs must not outrun the live split width).
 //
-// CTA layout (192 threads): warp 0 = TMA producer (one lane), warp 1 = MMA
-// issuer (one lane) and TMEM owner, warps 2..5 = epilogue, one accumulator row
-// per thread (warp w reads TMEM lanes 32*(w%4) .. +31).  Four smem stages of
-// A 128x64 + B 256x64 bf16 (48 KB each, 128-byte swizzle), two 128x256 fp32
-// accumulators in TMEM (all 512 columns) so the epilogue of tile i overlaps the
-// mainloop of tile i+1.  Every mbarrier wait is bounded; on expiry the CTA
-// raises an abort flag, drains its in-flight copies and MMAs, frees TMEM and
-// reports kStTimeout in the status word.
+// A launch carries up to kMaxTcJobs independent jobs (e.g. dW and dHidden of
+// chunk c next to the d-logits of chunk c+1).  Their tiles form one list that
+// the CTAs draw from through a global atomic counter, so a CTA that finishes
+// early takes more work and the jobs fill each other's tails.
+//
+// CTA layout (192 threads): warp 0 = tile fetcher + TMA producer (one lane),
+// warp 1 = MMA issuer (one lane) and TMEM owner, warps 2..5 = epilogue, one
+// accumulator row per thread (warp w reads TMEM lanes 32*(w%4) .. +31).  The
+// producer publishes each tile index in a small shared ring that the MMA and
+// epilogue roles read in order.  Four smem stages of A 128x64 + B 256x64 bf16
+// (48 KB each, 128-byte swizzle); two 128x256 fp32 accumulators in TMEM (all
+// 512 columns) so the epilogue of tile i overlaps the mainloop of tile i+1.
+// Every mbarrier wait is bounded; on expiry the CTA raises an abort flag,
+// drains its in-flight copies and MMAs, frees TMEM and reports kStTimeout.
 #include "eas_device.cuh"
 #include "eas_kernels.h"
 
@@ -31,12 +37,13 @@ namespace eas {
 namespace {
 
 constexpr int kStages = 4;
+constexpr int kRing = 4;                      // tile indices in flight
 constexpr int kABytes = kTcBM * kTcBK * 2;   // 16 KB
 constexpr int kBBytes = kTcBN * kTcBK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 256 /*barriers*/;
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 512 /*barriers*/;
 
 struct TileCoord {
   int m, n;
@@ -55,6 +62,26 @@ __device__ __forceinline__ TileCoord raster(int t, int num_m, int num_n, int gro
   c.m = m_first + in % gm;
   c.n = in / gm;
   return c;
+}
+
+// Per-job extents, identical in every thread.
+struct JobShape {
+  int num_m, num_n, num_kb, tiles, first;
+};
+
+struct Work {
+  int job;
+  TileCoord tc;
+};
+
+__device__ __forceinline__ Work locate(int t, const JobShape (&js)[kMaxTcJobs], int n_jobs,
+                                       const TcArgs& a) {
+  int j = 0;
+  while (j + 1 < n_jobs && t >= js[j + 1].first) ++j;
+  Work w;
+  w.job = j;
+  w.tc = raster(t - js[j].first, js[j].num_m, js[j].num_n, a.jobs[j].group_m > 0 ? a.jobs[j].group_m : 1);
+  return w;
 }
 
 // ------------------------------------------------------------ epilogues --
@@ -147,18 +174,19 @@ struct RowScalars {
 // d-logits of one row: dZ = g_lp (onehot - p) - g_H p (z - lse + H), p =
 // exp(z - lse), written as -p (g_H (z - lse) + g_lp + g_H H) + g_lp onehot.
 // Inactive rows and columns past the live width are written as exact zeros.
-__device__ __forceinline__ void epi_dlogits(const TcArgs& a, uint32_t tbase, bool k_empty,
-                                            int m_blk, int n_blk, int row, const RowScalars& rs) {
+__device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, uint32_t tbase,
+                                            bool k_empty, int m_blk, int n_blk, int row,
+                                            const RowScalars& rs) {
   const long long r = static_cast<long long>(m_blk) * kTcBM + row;
   const int n0 = n_blk * kTcBN;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.dz) + r * a.ldz + n0;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(jb.dz) + r * a.ldz + n0;
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 32; ++c) {
     uint32_t pk[16];
     const int col0 = n0 + c * 32;
     // tcgen05.ld is warp-collective: only warp-uniform conditions (live
     // width, empty K) may skip it; per-row activity is applied afterwards.
-    if (col0 >= a.vc_live) {
+    if (col0 >= jb.vc_live) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) pk[j] = 0u;
     } else {
@@ -173,7 +201,7 @@ __device__ __forceinline__ void epi_dlogits(const TcArgs& a, uint32_t tbase, boo
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = 0u;
       } else {
-        const int cvalid = a.vc_live - col0;
+        const int cvalid = jb.vc_live - col0;
         const int tj = rs.tgt - col0;
         float d[32];
 #pragma unroll
@@ -198,8 +226,9 @@ __device__ __forceinline__ void epi_dlogits(const TcArgs& a, uint32_t tbase, boo
 // dHidden: accumulate this chunk's product into the fp32 accumulator; the
 // last chunk converts to bf16 and scatters the row to its token (zeros for
 // gap rows whose mask byte is 0).
-__device__ __forceinline__ void epi_dhidden(const TcArgs& a, uint32_t tbase, bool k_empty,
-                                            int m_blk, int n_blk, int row, int tok, bool active) {
+__device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, uint32_t tbase,
+                                            bool k_empty, int m_blk, int n_blk, int row, int tok,
+                                            bool active) {
   const long long r = static_cast<long long>(m_blk) * kTcBM + row;
   const int n0 = n_blk * kTcBN;
   float* accp = a.acc + r * a.H + n0;
@@ -217,7 +246,7 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, uint32_t tbase, boo
       tmem_ld32(tbase + c * 32, v);
     }
     float4* ap = reinterpret_cast<float4*>(accp + c * 32);
-    if (!a.first_chunk) {
+    if (!jb.first_chunk) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float4 x = ap[q];
@@ -227,7 +256,7 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, uint32_t tbase, boo
         v[4 * q + 3] += x.w;
       }
     }
-    if (!a.last_chunk) {
+    if (!jb.last_chunk) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) ap[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     } else if (outp != nullptr) {
@@ -242,12 +271,12 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, uint32_t tbase, boo
 }
 
 // dW rows of this chunk: every vocabulary row of the chunk is overwritten.
-__device__ __forceinline__ void epi_dweight(const TcArgs& a, uint32_t tbase, bool k_empty,
-                                            int m_blk, int n_blk, int row) {
+__device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, uint32_t tbase,
+                                            bool k_empty, int m_blk, int n_blk, int row) {
   const int m = m_blk * kTcBM + row;
   const int n0 = n_blk * kTcBN;
-  const bool live = m < a.vc_live;
-  float* outp = a.dW + (static_cast<long long>(a.v0) + m) * a.H + n0;
+  const bool live = m < jb.vc_live;
+  float* outp = a.dW + (static_cast<long long>(jb.v0) + m) * a.H + n0;
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 32; ++c) {
     if (n0 + c * 32 >= a.H) break;
@@ -268,12 +297,7 @@ __device__ __forceinline__ void epi_dweight(const TcArgs& a, uint32_t tbase, boo
 
 // ----------------------------------------------------------------- kernel --
 
-template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
-  constexpr bool kAMN = (KIND == kTcDWeight);
-  constexpr bool kBMN = (KIND == kTcDHidden || KIND == kTcDWeight);
-  constexpr uint32_t kIdesc = idesc_bf16_f32(kTcBM, kTcBN, kAMN, kBMN);
-
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -283,8 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* rfull = tempty + 2;
+  uint64_t* rempty = rfull + kRing;
+  uint64_t* drain = rempty + kRing;
+  int* ring = reinterpret_cast<int*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + kRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -292,13 +319,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const Sched* sched = static_cast<const Sched*>(a.sched);
   DevStatus* st = static_cast<DevStatus*>(a.status);
 
-  const int M = a.M_fixed > 0 ? a.M_fixed : sched->R_pad;
-  const int K = a.K_fixed > 0 ? a.K_fixed : sched->R_pad;
-  const int num_m = (M + kTcBM - 1) / kTcBM;
-  const int num_n = (a.N + kTcBN - 1) / kTcBN;
-  const int num_kb = (K + kTcBK - 1) / kTcBK;
-  const int tiles = num_m * num_n;
-  const int group_m = a.group_m > 0 ? a.group_m : 1;
+  JobShape js[kMaxTcJobs];
+  int total = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTcJobs; ++j) {
+    js[j] = JobShape{0, 0, 0, 0, total};
+    if (j < a.n_jobs) {
+      const TcJob& jb = a.jobs[j];
+      const int M = jb.M_fixed > 0 ? jb.M_fixed : sched->R_pad;
+      const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R_pad;
+      js[j].num_m = (M + kTcBM - 1) / kTcBM;
+      js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
+      js[j].num_kb = (K + kTcBK - 1) / kTcBK;
+      js[j].tiles = js[j].num_m * js[j].num_n;
+      total += js[j].tiles;
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -309,14 +345,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 4);
     }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], 1 + 4);     // MMA thread + 4 epilogue warps
+    }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&a.tmA);
-    tma_prefetch_desc(&a.tmB);
+    for (int j = 0; j < a.n_jobs; ++j) {
+      tma_prefetch_desc(&a.jobs[j].tmA);
+      tma_prefetch_desc(&a.jobs[j].tmB);
+    }
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -325,16 +367,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
+    // ------------------------------------------------ tile fetcher + TMA producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
-        const TileCoord tc = raster(t, num_m, num_n, group_m);
-        for (int kb = 0; kb < num_kb; ++kb) {
+      for (int it = 0; ok; ++it) {
+        const int slot = it % kRing;
+        const uint32_t rph = (it / kRing) & 1;
+        if (!mbar_wait(&rempty[slot], rph ^ 1u, abort_flag, a.budget)) {
+          report(st, kStTimeout, 1, it);
+          ok = false;
+          break;
+        }
+        const int t = atomicAdd(a.tile_counter, 1);
+        ring[slot] = (t < total) ? t : -1;
+        mbar_arrive(&rfull[slot]);
+        if (t >= total) break;
+        const Work w = locate(t, js, a.n_jobs, a);
+        const TcJob& jb = a.jobs[w.job];
+        const int kind = jb.kind;
+        for (int kb = 0; kb < js[w.job].num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
-            report(st, kStTimeout, KIND * 16 + 1, t);
+            report(st, kStTimeout, 2, t);
             ok = false;
             break;
           }
@@ -342,21 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           uint8_t* dB = sB + stage * kBBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           const int k0 = kb * kTcBK;
-          if (KIND == kTcFwd || KIND == kTcDLogits) {
-            tma_load_2d(dA, &a.tmA, &full[stage], k0, tc.m * kTcBM);
-            tma_load_2d(dB, &a.tmB, &full[stage], k0, a.v0 + tc.n * kTcBN);
-          } else if (KIND == kTcDHidden) {
-            tma_load_2d(dA, &a.tmA, &full[stage], k0, tc.m * kTcBM);
+          if (kind == kTcFwd || kind == kTcDLogits) {
+            tma_load_2d(dA, &jb.tmA, &full[stage], k0, w.tc.m * kTcBM);
+            tma_load_2d(dB, &jb.tmB, &full[stage], k0, jb.v0 + w.tc.n * kTcBN);
+          } else if (kind == kTcDHidden) {
+            tma_load_2d(dA, &jb.tmA, &full[stage], k0, w.tc.m * kTcBM);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              tma_load_2d(dB + j * 8192, &a.tmB, &full[stage], tc.n * kTcBN + j * 64, a.v0 + k0);
+              tma_load_2d(dB + j * 8192, &jb.tmB, &full[stage], w.tc.n * kTcBN + j * 64, jb.v0 + k0);
           } else {
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              tma_load_2d(dA + j * 8192, &a.tmA, &full[stage], tc.m * kTcBM + j * 64, k0);
+              tma_load_2d(dA + j * 8192, &jb.tmA, &full[stage], w.tc.m * kTcBM + j * 64, k0);
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              tma_load_2d(dB + j * 8192, &a.tmB, &full[stage], tc.n * kTcBN + j * 64, k0);
+              tma_load_2d(dB + j * 8192, &jb.tmB, &full[stage], w.tc.n * kTcBN + j * 64, k0);
           }
           if (++stage == kStages) {
             stage = 0;
@@ -380,21 +435,37 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++it) {
+      for (int it = 0;; ++it) {
+        const int slot = it % kRing;
+        if (!mbar_wait(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
+          report(st, kStTimeout, 3, it);
+          break;
+        }
+        const int t = ring[slot];
+        mbar_arrive(&rempty[slot]);
+        if (t < 0) break;
+        const Work w = locate(t, js, a.n_jobs, a);
+        const int kind = a.jobs[w.job].kind;
+        const bool a_mn = (kind == kTcDWeight);
+        const bool b_mn = (kind == kTcDHidden || kind == kTcDWeight);
+        const uint32_t idesc = a_mn ? idesc_bf16_f32(kTcBM, kTcBN, true, true)
+                                    : (b_mn ? idesc_bf16_f32(kTcBM, kTcBN, false, true)
+                                            : idesc_bf16_f32(kTcBM, kTcBN, false, false));
+        const uint32_t a_lbo = a_mn ? 8192 : 16, a_step = a_mn ? 2048 : 32;
+        const uint32_t b_lbo = b_mn ? 8192 : 16, b_step = b_mn ? 2048 : 32;
         const int buf = it & 1;
         const uint32_t tph = (it >> 1) & 1;
         if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, a.budget)) {
-          report(st, kStTimeout, KIND * 16 + 2, t);
-          ok = false;
+          report(st, kStTimeout, 4, t);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * kTcBN;
+        const int num_kb = js[w.job].num_kb;
+        bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, a.budget)) {
-            report(st, kStTimeout, KIND * 16 + 3, t);
+            report(st, kStTimeout, 5, t);
             ok = false;
             break;
           }
@@ -403,11 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
-            const uint64_t adesc = kAMN ? sdesc_sw128(a_addr + k * 2048, 8192, 1024)
-                                        : sdesc_sw128(a_addr + k * 32, 16, 1024);
-            const uint64_t bdesc = kBMN ? sdesc_sw128(b_addr + k * 2048, 8192, 1024)
-                                        : sdesc_sw128(b_addr + k * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+            const uint64_t adesc = sdesc_sw128(a_addr + k * a_step, a_lbo, 1024);
+            const uint64_t bdesc = sdesc_sw128(b_addr + k * b_step, b_lbo, 1024);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -431,22 +500,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ------------------------------------------------ epilogue warps
     const int q = warp & 3;               // TMEM lane quarter of this warp
     const int row = q * 32 + lane;        // accumulator row of this thread
-    const bool k_empty = (num_kb == 0);
-    int it = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
-      const TileCoord tc = raster(t, num_m, num_n, group_m);
+    for (int it = 0;; ++it) {
+      const int slot = it % kRing;
+      if (!mbar_wait(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
+        report(st, kStTimeout, 6, it);
+        break;
+      }
+      const int t = ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&rempty[slot]);
+      if (t < 0) break;
+      const Work w = locate(t, js, a.n_jobs, a);
+      const TcJob& jb = a.jobs[w.job];
+      const int kind = jb.kind;
+      const bool k_empty = (js[w.job].num_kb == 0);
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
       // per-row operands, fetched before waiting on the accumulator
-      const long long r = static_cast<long long>(tc.m) * kTcBM + row;
+      const long long r = static_cast<long long>(w.tc.m) * kTcBM + row;
       int tok = -1;
-      if (KIND != kTcDWeight) tok = a.row_map[r];
+      if (kind != kTcDWeight) tok = a.row_map[r];
       int tgt = -1;
       RowScalars rs;
+      rs.active = false;
       bool active = false;
-      if (KIND == kTcFwd) {
+      if (kind == kTcFwd) {
         if (tok >= 0) tgt = a.targets[tok];
-      } else if (KIND == kTcDLogits) {
+      } else if (kind == kTcDLogits) {
         active = (tok >= 0) && (a.mask[tok] != 0);
         rs.active = active;
         if (active) {
@@ -455,22 +535,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           rs.gh2 = gh * kLn2;
           rs.c1 = fmaf(gh, h, gl);
           rs.glp = gl;
-          const int tg = a.targets[tok] - a.v0;
-          rs.tgt = (tg >= 0 && tg < a.vc_live) ? tg : -1;
+          const int tg = a.targets[tok] - jb.v0;
+          rs.tgt = (tg >= 0 && tg < jb.vc_live) ? tg : -1;
         }
-      } else if (KIND == kTcDHidden) {
+      } else if (kind == kTcDHidden) {
         active = (tok >= 0) && (a.mask[tok] != 0);
       }
       if (!mbar_wait(&tfull[buf], tph, abort_flag, a.budget)) {
-        report(st, kStTimeout, KIND * 16 + 4, t);
+        report(st, kStTimeout, 7, t);
         break;
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
-      if (KIND == kTcFwd) epi_fwd(a, tbase, k_empty, tc.m, tc.n, row, tgt);
-      if (KIND == kTcDLogits) epi_dlogits(a, tbase, k_empty, tc.m, tc.n, row, rs);
-      if (KIND == kTcDHidden) epi_dhidden(a, tbase, k_empty, tc.m, tc.n, row, tok, active);
-      if (KIND == kTcDWeight) epi_dweight(a, tbase, k_empty, tc.m, tc.n, row);
+      if (kind == kTcFwd) epi_fwd(a, tbase, k_empty, w.tc.m, w.tc.n, row, tgt);
+      else if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, w.tc.m, w.tc.n, row, rs);
+      else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, w.tc.m, w.tc.n, row, tok, active);
+      else epi_dweight(a, jb, tbase, k_empty, w.tc.m, w.tc.n, row);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -485,32 +565,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
 }
 
-template <int KIND>
-cudaError_t launch_kind(const TcArgs& args, int grid, cudaStream_t s) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<KIND>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
-  tc_gemm_kernel<KIND><<<grid, kThreads, kSmemBytes, s>>>(args);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 size_t tc_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
-  switch (args.kind) {
-    case kTcFwd: return launch_kind<kTcFwd>(args, grid, s);
-    case kTcDLogits: return launch_kind<kTcDLogits>(args, grid, s);
-    case kTcDHidden: return launch_kind<kTcDHidden>(args, grid, s);
-    case kTcDWeight: return launch_kind<kTcDWeight>(args, grid, s);
-    default: return cudaErrorInvalidValue;
+  if (args.n_jobs < 1 || args.n_jobs > kMaxTcJobs) return cudaErrorInvalidValue;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
   }
+  tc_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(args);
+  return cudaGetLastError();
 }
 
 }  // namespace eas

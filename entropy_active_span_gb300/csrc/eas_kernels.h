@@ -40,19 +40,35 @@ enum TcKind : int {
   kTcDWeight = 3,  // dW_c = dZ_c^T Hp -> fp32 dW rows
 };
 
-struct TcArgs {
+// One contraction of a launch.  A launch runs up to kMaxTcJobs jobs; their
+// tiles form one list (job 0's tiles first) that the CTAs draw from with an
+// atomic counter, so jobs with no dependency between them share the machine
+// and fill each other's tails.
+struct TcJob {
   CUtensorMap tmA;   // A operand (see TcKind for the layout of each kind)
   CUtensorMap tmB;   // B operand
-  const void* sched; // Sched*: packed row count R, R_pad
-  void* status;      // DevStatus*
-  long long budget;  // clocks before a pipeline wait gives up
   int kind;
   int M_fixed;       // > 0: rows of the problem; 0: R_pad from sched
   int N;             // columns of the problem
   int K_fixed;       // > 0: reduction length; 0: R_pad from sched
   int group_m;       // m-tiles per raster band
   int v0;            // first vocabulary row of the chunk (B row / k offset)
-  // epilogue operands
+  int vc_live;       // live columns of this chunk (dlogits / dweight)
+  int first_chunk;   // dhidden: first chunk (store, do not accumulate)
+  int last_chunk;    // dhidden: last chunk (convert and scatter to dhidden)
+  void* dz;          // dlogits: bf16 staging written by this job [T_pad][ldz]
+};
+
+constexpr int kMaxTcJobs = 3;
+
+struct TcArgs {
+  TcJob jobs[kMaxTcJobs];
+  int n_jobs;
+  const void* sched; // Sched*: packed row count R, R_pad
+  void* status;      // DevStatus*
+  int* tile_counter; // zero before the launch; one atomic per tile
+  long long budget;  // clocks before a pipeline wait gives up
+  // epilogue operands shared by the jobs
   const int* row_map;     // packed row -> token (or -1)
   const int* targets;     // [T]
   const uint8_t* mask;    // [T]
@@ -66,14 +82,10 @@ struct TcArgs {
   float* zt;              // [stride]
   long long part_stride;
   int V;                  // vocabulary size (fwd column bound)
-  int vc_live;            // live columns of this chunk (dlogits / dweight)
-  void* dz;               // bf16 staging [T_pad][ldz]
-  long long ldz;
+  long long ldz;          // staging row pitch
   float* acc;             // fp32 dHidden accumulator [T_pad][H]
   void* dhidden;          // bf16 [T][H]
   int H;
-  int first_chunk;
-  int last_chunk;
   float* dW;              // fp32 [V][H]
 };
 

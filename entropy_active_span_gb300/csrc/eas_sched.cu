@@ -271,49 +271,84 @@ gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
 // Folds the per-vocab-tile partials of each packed row into lse, entropy and
 // logp.  Partials are kept in base-2 units: with y = z log2(e), partial n of
 // row r holds, over the tile's valid columns, m = max y, s = sum 2^(y - m),
-// u = sum 2^(y - m) (y - m).  Merged in tile order:
-//   M = max m_n, S = sum s_n 2^(m_n - M), U = sum 2^(m_n - M) (u_n + (m_n - M) s_n)
-// so S = sum_v exp(z_v - M ln2) and U ln2 = sum_v exp(z_v - M ln2) (z_v - M ln2):
+// u = sum 2^(y - m) (y - m).  Two states merge as
+//   M = max(m_a, m_b), S = sum_i s_i 2^(m_i - M), U = sum_i 2^(m_i - M) (u_i + (m_i - M) s_i)
+// so that S = sum_v exp(z_v - M ln2) and U ln2 = sum_v exp(z_v - M ln2) (z_v - M ln2):
 //   lse = M ln2 + log S,  H = log S - (U / S) ln2,  logp = z_target - lse.
-// Tokens without a packed row, or with mask 0, get zeros.
-__global__ void __launch_bounds__(256)
+// A block handles 32 tokens; its 8 thread groups fold the tiles n = g, g+8,
+// ... of each token (coalesced across the 32 tokens), then group 0 merges the
+// 8 states in a fixed order.  Tokens without a packed row, or with mask 0,
+// get zeros.
+namespace {
+constexpr int kCombTok = 32;
+constexpr int kCombGroups = 8;
+
+struct Lse3 {
+  float m, s, u;
+};
+
+__device__ __forceinline__ void lse_merge(Lse3& a, float m, float s, float u) {
+  if (s == 0.f) return;
+  if (a.s == 0.f) {
+    a.m = m; a.s = s; a.u = u;
+    return;
+  }
+  if (m > a.m) {
+    const float d = a.m - m;               // < 0
+    const float f = ex2_approx(d);
+    a.u = f * (a.u + d * a.s) + u;
+    a.s = f * a.s + s;
+    a.m = m;
+  } else {
+    const float d = m - a.m;               // <= 0
+    const float f = ex2_approx(d);
+    a.s += f * s;
+    a.u += f * (u + d * s);
+  }
+}
+}  // namespace
+
+__global__ void __launch_bounds__(kCombTok * kCombGroups)
 combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
                const float* __restrict__ pu, const float* __restrict__ zt, int n_tiles,
                long long stride, const int* __restrict__ pack_of, const uint8_t* __restrict__ mask,
                long long T, float* __restrict__ logprob, float* __restrict__ entropy,
                float* __restrict__ lse) {
-  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < T;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int r = pack_of[t];
-    if (r < 0 || mask[t] == 0) {
-      logprob[t] = 0.f;
-      entropy[t] = 0.f;
-      lse[t] = 0.f;
-      continue;
+  __shared__ Lse3 st[kCombGroups][kCombTok];
+  const int x = threadIdx.x % kCombTok, g = threadIdx.x / kCombTok;
+  for (long long t0 = static_cast<long long>(blockIdx.x) * kCombTok; t0 < T;
+       t0 += static_cast<long long>(gridDim.x) * kCombTok) {
+    const long long t = t0 + x;
+    int r = -1;
+    if (t < T) {
+      r = pack_of[t];
+      if (r >= 0 && mask[t] == 0) r = -1;
     }
-    float M = pm[r], S = ps[r], U = pu[r];
-    for (int n = 1; n < n_tiles; ++n) {
-      const float m = pm[n * stride + r];
-      const float s = ps[n * stride + r];
-      const float u = pu[n * stride + r];
-      if (m > M) {
-        const float d = M - m;                 // < 0
-        const float f = ex2_approx(d);
-        U = f * (U + d * S) + u;
-        S = f * S + s;
-        M = m;
-      } else {
-        const float d = m - M;                 // <= 0
-        const float f = ex2_approx(d);
-        S += f * s;
-        U += f * (u + d * s);
+    Lse3 a{0.f, 0.f, 0.f};
+    if (r >= 0) {
+      for (int n = g; n < n_tiles; n += kCombGroups) {
+        const long long o = n * stride + r;
+        lse_merge(a, pm[o], ps[o], pu[o]);
       }
     }
-    const float logS = logf(S);
-    const float l = fmaf(M, kLn2, logS);
-    lse[t] = l;
-    entropy[t] = logS - (U / S) * kLn2;
-    logprob[t] = zt[r] - l;
+    st[g][x] = a;
+    __syncthreads();
+    if (g == 0 && t < T) {
+      if (r < 0) {
+        logprob[t] = 0.f;
+        entropy[t] = 0.f;
+        lse[t] = 0.f;
+      } else {
+        Lse3 acc = st[0][x];
+        for (int k = 1; k < kCombGroups; ++k) lse_merge(acc, st[k][x].m, st[k][x].s, st[k][x].u);
+        const float logS = logf(acc.s);
+        const float l = fmaf(acc.m, kLn2, logS);
+        lse[t] = l;
+        entropy[t] = logS - (acc.u / acc.s) * kLn2;
+        logprob[t] = zt[r] - l;
+      }
+    }
+    __syncthreads();
   }
 }
 
@@ -359,9 +394,9 @@ cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, co
                            long long T, float* logprob, float* entropy, float* lse, int num_sms,
                            cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  long long grid = (T + 255) / 256;
-  if (grid > 16LL * num_sms) grid = 16LL * num_sms;
-  combine_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(pm, ps, pu, zt, n_tiles, stride,
+  long long grid = (T + kCombTok - 1) / kCombTok;
+  if (grid > 32LL * num_sms) grid = 32LL * num_sms;
+  combine_kernel<<<static_cast<unsigned>(grid), kCombTok * kCombGroups, 0, s>>>(pm, ps, pu, zt, n_tiles, stride,
                                                              pack_of, mask, T, logprob, entropy,
                                                              lse);
   return cudaGetLastError();

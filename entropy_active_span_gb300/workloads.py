@@ -72,6 +72,10 @@ PROFILE_WORKLOADS = {
     "rl_4k_v32k": Workload(
         "rl_4k_v32k", 4096, 4096, 32768, "bf16", 1102, "rl_prompts_1024",
         description="T=4096 H=4096 V=32768 bf16; 4 sequences x 1024, prompt 256..512 inactive"),
+    "rl_16k_v32k": Workload(
+        "rl_16k_v32k", 16384, 4096, 32768, "bf16", 1002, "rl_prompts_1024",
+        description="rl_16k's rows and mask with V=32768: its backward launches have the "
+                    "shapes of rl_16k's (about 2 GB on the device)"),
 }
 ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
 
