@@ -88,6 +88,26 @@ def peaks():
     return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
 
 
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, or None.
+
+    Summaries under profiles/ carry lines 'traffic <kernel> <bytes> <sha>'
+    where sha is sha256[:16] of the tensor-core kernel sources at capture
+    time; a figure taken from an older kernel is not reported."""
+    import glob
+    import hashlib
+    csrc = os.path.join(ROOT, "entropy_active_span_gb300", "csrc")
+    src = "".join(open(os.path.join(csrc, f)).read()
+                  for f in ("eas_gemm_tc.cu", "eas_device.cuh", "eas_kernels.h"))
+    sha = hashlib.sha256(src.encode()).hexdigest()[:16]
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for line in open(path):
+            parts = line.split()
+            if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel and parts[3] == sha:
+                return int(parts[2])
+    return None
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -339,7 +359,7 @@ def main():
         achieved = flops_kind / (tot_ms / 1000.0) / 1e12
         roofline = {"bound": "tensor", "kernel": name, "achieved": achieved,
                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": achieved / pk["bf16_sustained"], "traffic": None,
+                    "frac": achieved / pk["bf16_sustained"], "traffic": recorded_traffic(name),
                     "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
                     "launches_per_step": count / args.steps,
                     "ms_per_launch": tot_ms / count}

@@ -204,7 +204,7 @@ size_t align_up(size_t x) { return (x + 1023) / 1024 * 1024; }
 Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chunk) {
   Layout L;
   const size_t esz = (dt == EAS_BF16) ? 2 : 4;
-  L.T_pad = round_up(T, 128);
+  L.T_pad = round_up(T, 256);
   L.vt = (dt == EAS_BF16) ? kTcBN : kSimtBN;
   L.n_vt = static_cast<int>(cdiv(V, L.vt));
   if (chunk <= 0) chunk = EAS_DEFAULT_VOCAB_CHUNK;
@@ -359,7 +359,7 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
   st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, ws, L, di, s);
   if (st != EAS_OK || T == 0) return st;
   const Sched* sched = at<Sched>(ws, L.sched);
-  const long long num_m_max = L.T_pad / 128;
+  const long long num_m_max = L.T_pad / tc_tile_rows();
 
   if (dtype == EAS_BF16) {
     TcArgs a;
@@ -367,13 +367,13 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
     TcJob& j = a.jobs[0];
     st = make_map_bf16(&j.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128);
     if (st != EAS_OK) return st;
-    st = make_map_bf16(&j.tmB, weight, H, V, H, 256);
+    st = make_map_bf16(&j.tmB, weight, H, V, H, tc_tile_rows() == 256 ? 128 : 256);
     if (st != EAS_OK) return st;
     j.kind = kTcFwd;
     j.M_fixed = 0;
     j.N = static_cast<int>(V);
     j.K_fixed = static_cast<int>(H);
-    j.group_m = group_for(128LL * H * 2, num_m_max);
+    j.group_m = group_for(tc_tile_rows() * H * 2LL, num_m_max);
     a.n_jobs = 1;
     a.sched = sched;
     a.status = at<DevStatus>(ws, L.status);
@@ -469,7 +469,7 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
              "zero rows");
   }
   const Sched* sched = at<Sched>(ws, L.sched);
-  const long long num_m_max = L.T_pad / 128;
+  const long long num_m_max = L.T_pad / tc_tile_rows();
 
   if (dtype == EAS_BF16) {
     // Launch c (0..n) runs dW and dHidden of chunk c-1 (reading staging
@@ -478,7 +478,8 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
     // launch boundary orders a chunk's d-logits before its projections.
     CUtensorMap hp_k, w_k, w_mn, hp_mn;
     if ((st = make_map_bf16(&hp_k, at<char>(ws, L.hp), H, L.T_pad, H, 128)) != EAS_OK) return st;
-    if ((st = make_map_bf16(&w_k, weight, H, V, H, 256)) != EAS_OK) return st;
+    if ((st = make_map_bf16(&w_k, weight, H, V, H, tc_tile_rows() == 256 ? 128 : 256)) != EAS_OK)
+      return st;
     if ((st = make_map_bf16(&w_mn, weight, H, V, H, 64)) != EAS_OK) return st;
     if ((st = make_map_bf16(&hp_mn, at<char>(ws, L.hp), H, L.T_pad, H, 64)) != EAS_OK) return st;
     TcArgs base;
@@ -522,10 +523,10 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
         w.M_fixed = static_cast<int>(live);
         w.N = static_cast<int>(H);
         w.K_fixed = 0;
-        w.group_m = group_for(128LL * L.T_pad * 2, cdiv(live, kTcBM));
+        w.group_m = group_for(tc_tile_rows() * L.T_pad * 2LL, cdiv(live, tc_tile_rows()));
         w.v0 = static_cast<int>(v0);
         w.vc_live = static_cast<int>(live);
-        tiles += cdiv(live, kTcBM) * cdiv(H, kTcBN);
+        tiles += cdiv(live, tc_tile_rows()) * cdiv(H, kTcBN);
         TcJob& h = a.jobs[a.n_jobs++];
         h.tmA = dz_k;
         h.tmB = w_mn;
@@ -533,7 +534,7 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
         h.M_fixed = 0;
         h.N = static_cast<int>(H);
         h.K_fixed = static_cast<int>(live);
-        h.group_m = group_for(128LL * live * 2, num_m_max);
+        h.group_m = group_for(tc_tile_rows() * live * 2LL, num_m_max);
         h.v0 = static_cast<int>(v0);
         h.vc_live = static_cast<int>(live);
         h.first_chunk = (p == 0);
@@ -551,7 +552,7 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
         d.M_fixed = 0;
         d.N = static_cast<int>(live);
         d.K_fixed = static_cast<int>(H);
-        d.group_m = group_for(128LL * H * 2, num_m_max);
+        d.group_m = group_for(tc_tile_rows() * H * 2LL, num_m_max);
         d.v0 = static_cast<int>(v0);
         d.vc_live = static_cast<int>(live);
         d.dz = staging[c % 2];

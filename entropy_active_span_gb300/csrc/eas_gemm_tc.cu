@@ -17,18 +17,24 @@
 //
 // A launch carries up to kMaxTcJobs independent jobs (e.g. dW and dHidden of
 // chunk c next to the d-logits of chunk c+1).  Their tiles form one list that
-// the CTAs draw from through a global atomic counter, so a CTA that finishes
-// early takes more work and the jobs fill each other's tails.
+// the CTA pairs draw from through a global atomic counter, so a pair that
+// finishes early takes more work and the jobs fill each other's tails.
 //
-// CTA layout (192 threads): warp 0 = tile fetcher + TMA producer (one lane),
-// warp 1 = MMA issuer (one lane) and TMEM owner, warps 2..5 = epilogue, one
-// accumulator row per thread (warp w reads TMEM lanes 32*(w%4) .. +31).  The
-// producer publishes each tile index in a small shared ring that the MMA and
-// epilogue roles read in order.  Four smem stages of A 128x64 + B 256x64 bf16
-// (48 KB each, 128-byte swizzle); two 128x256 fp32 accumulators in TMEM (all
-// 512 columns) so the epilogue of tile i overlaps the mainloop of tile i+1.
-// Every mbarrier wait is bounded; on expiry the CTA raises an abort flag,
-// drains its in-flight copies and MMAs, frees TMEM and reports kStTimeout.
+// Tiles are 256 x 256 and computed by a cluster of two CTAs (the two SMs of a
+// TPC) with tcgen05.mma.cta_group::2: CTA r loads A rows [128r, 128r+128) and
+// B columns [128r, 128r+128) of the tile (32 KB per k-step of 64, six stages),
+// and each CTA's TMEM receives its 128 x 256 half of the accumulator.  CTA
+// layout (192 threads): warp 0 = TMA producer (lane 0; on the even CTA it also
+// fetches tile indices and publishes them to both CTAs), warp 1 = MMA issuer
+// (lane 0 of the even CTA) and TMEM owner, warps 2..5 = epilogue, one
+// accumulator row per thread (warp w reads TMEM lanes 32*(w%4) .. +31).  Two
+// 256-column fp32 accumulators per CTA (all 512 TMEM columns) let the epilogue
+// of tile i overlap the mainloop of tile i+1.  Every mbarrier wait is bounded;
+// on expiry a CTA raises its abort flag, lets its in-flight copies and MMAs
+// land, frees TMEM and reports kStTimeout in the status word.
+#include <cstdlib>
+#include <cstring>
+
 #include "eas_device.cuh"
 #include "eas_kernels.h"
 
@@ -36,14 +42,9 @@ namespace eas {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kRing = 4;                      // tile indices in flight
-constexpr int kABytes = kTcBM * kTcBK * 2;   // 16 KB
-constexpr int kBBytes = kTcBN * kTcBK * 2;   // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align slack*/ + 512 /*barriers*/;
 
 struct TileCoord {
   int m, n;
@@ -89,8 +90,8 @@ __device__ __forceinline__ Work locate(int t, const JobShape (&js)[kMaxTcJobs], 
 // Forward: per-row online softmax statistics over the tile's valid columns,
 // in base-2 units (y = z log2 e): m = max y, s = sum 2^(y-m), u = sum
 // 2^(y-m)(y-m); plus the target logit when the target falls in this tile.
-__device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_empty, int m_blk,
-                                        int n_blk, int row, int tgt) {
+__device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_empty,
+                                        long long r0, int n_blk, int row, int tgt) {
   const int n0 = n_blk * kTcBN;
   int valid = a.V - n0;
   if (valid > kTcBN) valid = kTcBN;
@@ -154,7 +155,7 @@ __device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_
       }
     }
   }
-  const long long r = static_cast<long long>(m_blk) * kTcBM + row;
+  const long long r = r0 + row;
   const long long o = static_cast<long long>(n_blk) * a.part_stride + r;
   a.part_m[o] = m2;
   a.part_s[o] = s;
@@ -175,9 +176,9 @@ struct RowScalars {
 // exp(z - lse), written as -p (g_H (z - lse) + g_lp + g_H H) + g_lp onehot.
 // Inactive rows and columns past the live width are written as exact zeros.
 __device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, uint32_t tbase,
-                                            bool k_empty, int m_blk, int n_blk, int row,
+                                            bool k_empty, long long r0, int n_blk, int row,
                                             const RowScalars& rs) {
-  const long long r = static_cast<long long>(m_blk) * kTcBM + row;
+  const long long r = r0 + row;
   const int n0 = n_blk * kTcBN;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(jb.dz) + r * a.ldz + n0;
 #pragma unroll 1
@@ -227,9 +228,9 @@ __device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, ui
 // last chunk converts to bf16 and scatters the row to its token (zeros for
 // gap rows whose mask byte is 0).
 __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, uint32_t tbase,
-                                            bool k_empty, int m_blk, int n_blk, int row, int tok,
+                                            bool k_empty, long long r0, int n_blk, int row, int tok,
                                             bool active) {
-  const long long r = static_cast<long long>(m_blk) * kTcBM + row;
+  const long long r = r0 + row;
   const int n0 = n_blk * kTcBN;
   float* accp = a.acc + r * a.H + n0;
   __nv_bfloat16* outp =
@@ -272,8 +273,8 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, ui
 
 // dW rows of this chunk: every vocabulary row of the chunk is overwritten.
 __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, uint32_t tbase,
-                                            bool k_empty, int m_blk, int n_blk, int row) {
-  const int m = m_blk * kTcBM + row;
+                                            bool k_empty, long long r0, int n_blk, int row) {
+  const int m = static_cast<int>(r0) + row;
   const int n0 = n_blk * kTcBN;
   const bool live = m < jb.vc_live;
   float* outp = a.dW + (static_cast<long long>(jb.v0) + m) * a.H + n0;
@@ -297,15 +298,127 @@ __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, ui
 
 // ----------------------------------------------------------------- kernel --
 
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcArgs a) {
+// =====================================================================
+// The CTA-pair kernel.  Against one CTA per 128 x 256 tile, the pair halves
+// the B bytes each SM moves from L2 and reads from shared memory per k-step.
+//
+// Synchronisation (each line: barrier, where it lives, who arrives):
+//   full[s]   leader   leader producer's expect_tx (64 KB) + both CTAs' TMA bytes
+//   empty[s]  both     leader MMA commit, multicast to both CTAs
+//   tfull[b]  both     leader MMA commit, multicast to both CTAs
+//   tempty[b] leader   4 epilogue warps of each CTA (the peer's arrive remotely)
+//   rfull[i]  both     leader fetcher (local arrive + remote arrive)
+//   rempty[i] leader   leader MMA + 4 leader epilogue warps + peer producer
+//                      + 4 peer epilogue warps
+// =====================================================================
+
+constexpr int kPStages = 6;
+constexpr int kPHalf = 128;                       // rows (of A) / columns (of B) per CTA
+constexpr int kPM = 256;                          // rows of a pair tile
+constexpr int kPABytes = kPHalf * kTcBK * 2;      // 16 KB
+constexpr int kPBBytes = kPHalf * kTcBK * 2;      // 16 KB
+constexpr int kPStageBytes = kPABytes + kPBBytes; // 32 KB per CTA
+constexpr int kPSmemBytes = kPStages * kPStageBytes + 1024 + 512;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Shared::cluster address of the same shared-memory location in CTA `rank`.
+__device__ __forceinline__ uint32_t map_rank(const void* p, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+  return out;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cl(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait with cluster-scope acquire (for barriers other CTAs arrive on).
+__device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                             long long budget) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > budget) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// TMA load into this CTA's shared memory whose completion bytes are counted
+// on a barrier of either CTA of the pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when
+// the pair MMAs issued so far complete.
+__device__ __forceinline__ void umma_commit_pair_both(uint64_t* bar) {
+  const uint16_t mask = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint8_t* sB = smem + kPStages * kPABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPStages * kPBBytes);
+  uint64_t* empty = full + kPStages;
+  uint64_t* tfull = empty + kPStages;
   uint64_t* tempty = tfull + 2;
   uint64_t* rfull = tempty + 2;
   uint64_t* rempty = rfull + kRing;
@@ -316,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = (rank == 0);
   const Sched* sched = static_cast<const Sched*>(a.sched);
   DevStatus* st = static_cast<DevStatus*>(a.status);
 
@@ -328,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const TcJob& jb = a.jobs[j];
       const int M = jb.M_fixed > 0 ? jb.M_fixed : sched->R_pad;
       const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R_pad;
-      js[j].num_m = (M + kTcBM - 1) / kTcBM;
+      js[j].num_m = (M + kPM - 1) / kPM;
       js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
       js[j].num_kb = (K + kTcBK - 1) / kTcBK;
       js[j].tiles = js[j].num_m * js[j].num_n;
@@ -337,17 +452,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   }
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kPStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], 8);
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&rfull[i], 1);
-      mbar_init(&rempty[i], 1 + 4);     // MMA thread + 4 epilogue warps
+      mbar_init(&rempty[i], 10);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -360,14 +475,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       tma_prefetch_desc(&a.jobs[j].tmB);
     }
   }
-  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();     // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // shared::cluster addresses of the leader's barriers and the peer's ring
+  const uint32_t full_leader0 = map_rank(&full[0], 0);
+  const uint32_t tempty_leader0 = map_rank(&tempty[0], 0);
+  const uint32_t rempty_leader0 = map_rank(&rempty[0], 0);
+  const uint32_t ring_peer0 = map_rank(&ring[0], 1);
+  const uint32_t rfull_peer0 = map_rank(&rfull[0], 1);
+
   if (warp == 0) {
-    // ------------------------------------------------ tile fetcher + TMA producer
+    // ------------------------------------------------ fetcher (leader) + TMA producer (both)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
@@ -375,70 +503,85 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       for (int it = 0; ok; ++it) {
         const int slot = it % kRing;
         const uint32_t rph = (it / kRing) & 1;
-        if (!mbar_wait(&rempty[slot], rph ^ 1u, abort_flag, a.budget)) {
-          report(st, kStTimeout, 1, it);
-          ok = false;
-          break;
-        }
-        const int t = atomicAdd(a.tile_counter, 1);
-        ring[slot] = (t < total) ? t : -1;
-        mbar_arrive(&rfull[slot]);
-        if (t >= total) break;
-        const Work w = locate(t, js, a.n_jobs, a);
-        const TcJob& jb = a.jobs[w.job];
-        const int kind = jb.kind;
-        for (int kb = 0; kb < js[w.job].num_kb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
-            report(st, kStTimeout, 2, t);
+        int t;
+        if (leader) {
+          if (!mbar_wait_cl(&rempty[slot], rph ^ 1u, abort_flag, a.budget)) {
+            report(st, kStTimeout, 11, it);
             ok = false;
             break;
           }
-          uint8_t* dA = sA + stage * kABytes;
-          uint8_t* dB = sB + stage * kBBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          const int got = atomicAdd(a.tile_counter, 1);
+          t = (got < total) ? got : -1;
+          ring[slot] = t;
+          st_cluster_u32(ring_peer0 + 4 * slot, static_cast<uint32_t>(t));
+          mbar_arrive(&rfull[slot]);
+          mbar_arrive_cluster(rfull_peer0 + 8 * slot);
+        } else {
+          if (!mbar_wait_cl(&rfull[slot], rph, abort_flag, a.budget)) {
+            report(st, kStTimeout, 12, it);
+            ok = false;
+            break;
+          }
+          t = ring[slot];
+          mbar_arrive_cluster(rempty_leader0 + 8 * slot);
+        }
+        if (t < 0) break;
+        const Work w = locate(t, js, a.n_jobs, a);
+        const TcJob& jb = a.jobs[w.job];
+        const int kind = jb.kind;
+        const int mrow = w.tc.m * kPM + static_cast<int>(rank) * kPHalf;   // this CTA's A rows
+        const int ncol = w.tc.n * kTcBN + static_cast<int>(rank) * kPHalf; // this CTA's B columns
+        for (int kb = 0; kb < js[w.job].num_kb; ++kb) {
+          if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
+            report(st, kStTimeout, 13, t);
+            ok = false;
+            break;
+          }
+          uint8_t* dA = sA + stage * kPABytes;
+          uint8_t* dB = sB + stage * kPBBytes;
+          const uint32_t bar = full_leader0 + 8 * stage;
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPStageBytes);
           const int k0 = kb * kTcBK;
           if (kind == kTcFwd || kind == kTcDLogits) {
-            tma_load_2d(dA, &jb.tmA, &full[stage], k0, w.tc.m * kTcBM);
-            tma_load_2d(dB, &jb.tmB, &full[stage], k0, jb.v0 + w.tc.n * kTcBN);
+            tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
+            tma_load_2d_pair(dB, &jb.tmB, bar, k0, jb.v0 + ncol);
           } else if (kind == kTcDHidden) {
-            tma_load_2d(dA, &jb.tmA, &full[stage], k0, w.tc.m * kTcBM);
+            tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(dB + j * 8192, &jb.tmB, &full[stage], w.tc.n * kTcBN + j * 64, jb.v0 + k0);
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(dB + j * 8192, &jb.tmB, bar, ncol + j * 64, jb.v0 + k0);
           } else {
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-              tma_load_2d(dA + j * 8192, &jb.tmA, &full[stage], w.tc.m * kTcBM + j * 64, k0);
+              tma_load_2d_pair(dA + j * 8192, &jb.tmA, bar, mrow + j * 64, k0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(dB + j * 8192, &jb.tmB, &full[stage], w.tc.n * kTcBN + j * 64, k0);
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d_pair(dB + j * 8192, &jb.tmB, bar, ncol + j * 64, k0);
           }
-          if (++stage == kStages) {
+          if (++stage == kPStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {
-        // Let every copy this thread issued land before the CTA exits: the
-        // last use of stage s had parity `phase` if s < stage, else phase^1.
-        for (int s = 0; s < kStages; ++s) {
-          const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+      if (!ok && leader) {
+        for (int s2 = 0; s2 < kPStages; ++s2) {
+          const uint32_t par = (s2 < stage) ? phase : (phase ^ 1u);
           long long t0 = clock64();
-          while (!mbar_try_wait(&full[s], par) && clock64() - t0 < a.budget) {
+          while (!mbar_try_wait_cl(&full[s2], par) && clock64() - t0 < a.budget) {
           }
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------ MMA issuer (leader only)
+    if (leader && lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       for (int it = 0;; ++it) {
         const int slot = it % kRing;
-        if (!mbar_wait(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
-          report(st, kStTimeout, 3, it);
+        if (!mbar_wait_cl(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
+          report(st, kStTimeout, 14, it);
           break;
         }
         const int t = ring[slot];
@@ -448,15 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const int kind = a.jobs[w.job].kind;
         const bool a_mn = (kind == kTcDWeight);
         const bool b_mn = (kind == kTcDHidden || kind == kTcDWeight);
-        const uint32_t idesc = a_mn ? idesc_bf16_f32(kTcBM, kTcBN, true, true)
-                                    : (b_mn ? idesc_bf16_f32(kTcBM, kTcBN, false, true)
-                                            : idesc_bf16_f32(kTcBM, kTcBN, false, false));
+        const uint32_t idesc = a_mn ? idesc_bf16_f32(kPM, kTcBN, true, true)
+                                    : (b_mn ? idesc_bf16_f32(kPM, kTcBN, false, true)
+                                            : idesc_bf16_f32(kPM, kTcBN, false, false));
         const uint32_t a_lbo = a_mn ? 8192 : 16, a_step = a_mn ? 2048 : 32;
         const uint32_t b_lbo = b_mn ? 8192 : 16, b_step = b_mn ? 2048 : 32;
         const int buf = it & 1;
         const uint32_t tph = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, a.budget)) {
-          report(st, kStTimeout, 4, t);
+        if (!mbar_wait_cl(&tempty[buf], tph ^ 1u, abort_flag, a.budget)) {
+          report(st, kStTimeout, 15, t);
           break;
         }
         tc_fence_after();
@@ -464,51 +607,55 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         const int num_kb = js[w.job].num_kb;
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, a.budget)) {
-            report(st, kStTimeout, 5, t);
+          if (!mbar_wait_cl(&full[stage], phase, abort_flag, a.budget)) {
+            report(st, kStTimeout, 16, t);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kBBytes);
+          const uint32_t a_addr = smem_u32(sA + stage * kPABytes);
+          const uint32_t b_addr = smem_u32(sB + stage * kPBBytes);
 #pragma unroll
           for (int k = 0; k < kTcBK / 16; ++k) {
             const uint64_t adesc = sdesc_sw128(a_addr + k * a_step, a_lbo, 1024);
             const uint64_t bdesc = sdesc_sw128(b_addr + k * b_step, b_lbo, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);
-          if (++stage == kStages) {
+          umma_commit_pair_both(&empty[stage]);
+          if (++stage == kPStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (num_kb == 0)
+        if (num_kb == 0) {
           mbar_arrive(&tfull[buf]);
-        else
-          umma_commit(&tfull[buf]);
+          mbar_arrive_cluster(map_rank(&tfull[buf], 1));
+        } else {
+          umma_commit_pair_both(&tfull[buf]);
+        }
       }
-      // Wait for every MMA this thread issued before TMEM is released.
-      umma_commit(drain);
+      umma_commit_pair_local(drain);
       long long t0 = clock64();
       while (!mbar_try_wait(drain, 0) && clock64() - t0 < a.budget) {
       }
     }
   } else {
-    // ------------------------------------------------ epilogue warps
-    const int q = warp & 3;               // TMEM lane quarter of this warp
-    const int row = q * 32 + lane;        // accumulator row of this thread
+    // ------------------------------------------------ epilogue warps (both CTAs)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
-      if (!mbar_wait(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
-        report(st, kStTimeout, 6, it);
+      if (!mbar_wait_cl(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
+        report(st, kStTimeout, 17, it);
         break;
       }
       const int t = ring[slot];
       __syncwarp();
-      if (lane == 0) mbar_arrive(&rempty[slot]);
+      if (lane == 0) {
+        if (leader) mbar_arrive(&rempty[slot]);
+        else mbar_arrive_cluster(rempty_leader0 + 8 * slot);
+      }
       if (t < 0) break;
       const Work w = locate(t, js, a.n_jobs, a);
       const TcJob& jb = a.jobs[w.job];
@@ -516,8 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const bool k_empty = (js[w.job].num_kb == 0);
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
-      // per-row operands, fetched before waiting on the accumulator
-      const long long r = static_cast<long long>(w.tc.m) * kTcBM + row;
+      const long long r0 = static_cast<long long>(w.tc.m) * kPM + static_cast<long long>(rank) * kPHalf;
+      const long long r = r0 + row;
       int tok = -1;
       if (kind != kTcDWeight) tok = a.row_map[r];
       int tgt = -1;
@@ -541,46 +688,66 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       } else if (kind == kTcDHidden) {
         active = (tok >= 0) && (a.mask[tok] != 0);
       }
-      if (!mbar_wait(&tfull[buf], tph, abort_flag, a.budget)) {
-        report(st, kStTimeout, 7, t);
+      if (!mbar_wait_cl(&tfull[buf], tph, abort_flag, a.budget)) {
+        report(st, kStTimeout, 18, t);
         break;
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
-      if (kind == kTcFwd) epi_fwd(a, tbase, k_empty, w.tc.m, w.tc.n, row, tgt);
-      else if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, w.tc.m, w.tc.n, row, rs);
-      else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, w.tc.m, w.tc.n, row, tok, active);
-      else epi_dweight(a, jb, tbase, k_empty, w.tc.m, w.tc.n, row);
+      if (kind == kTcFwd) epi_fwd(a, tbase, k_empty, r0, w.tc.n, row, tgt);
+      else if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, r0, w.tc.n, row, rs);
+      else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
+      else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (lane == 0) {
+        if (leader) mbar_arrive(&tempty[buf]);
+        else mbar_arrive_cluster(tempty_leader0 + 8 * buf);
+      }
     }
   }
 
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();     // both CTAs done with TMEM and with each other's barriers
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
   }
 }
 
 }  // namespace
 
-size_t tc_smem_bytes() { return kSmemBytes; }
+size_t tc_smem_bytes() { return kPSmemBytes; }
+
+int tc_tile_rows() { return kPM; }
 
 cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (args.n_jobs < 1 || args.n_jobs > kMaxTcJobs) return cudaErrorInvalidValue;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  tc_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(args);
-  return cudaGetLastError();
+  const int clusters = (grid + 1) / 2;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kPSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_pair_kernel, args);
 }
 
 }  // namespace eas

@@ -27,9 +27,9 @@ cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T
 
 // ---- tcgen05 GEMMs with fused epilogues, bf16 (eas_gemm_tc.cu) ----
 
-// Tile shape of every tensor-core GEMM: 128 x 256 accumulator in TMEM, K in
-// blocks of 64 bf16 (one 128-byte swizzle row).
-constexpr int kTcBM = 128;
+// Tensor-core tiles: 256 x 256 outputs per CTA pair (128 x 256 per CTA in
+// TMEM), K in blocks of 64 bf16 (one 128-byte swizzle row).
+constexpr int kTcBM = 128;    // accumulator rows held by one CTA
 constexpr int kTcBN = 256;
 constexpr int kTcBK = 64;
 
@@ -90,6 +90,8 @@ struct TcArgs {
 };
 
 size_t tc_smem_bytes();
+// Rows of one tensor-core tile (256 for the CTA-pair kernel, else 128).
+int tc_tile_rows();
 cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s);
 
 // ---- fp32 SIMT GEMMs with the same epilogues (eas_simt.cu) ----

@@ -152,7 +152,8 @@ spans_build_kernel(const uint8_t* __restrict__ mask, long long T, int max_gap,
 }
 
 // Validates the spans and lists the rows the kernels work on, in span order:
-//   row_map[r] = token of packed row r (r < R), -1 for r in [R, R_pad);
+//   row_map[r] = token of packed row r (r < R), -1 for r in [R, R_pad), R_pad =
+//   R rounded up to 256 (a whole number of tensor-core tiles of either shape);
 //   pack_of[t] = packed row of token t, or -1.
 // A row is listed when it lies in a span and (policy EAS_ROWS_SPAN, or the
 // token is active).  Spans must be sorted, disjoint, inside [0, T) and cover
@@ -240,7 +241,7 @@ rowmap_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
     }
     return;
   }
-  const long long R_pad = (R + 127) / 128 * 128;
+  const long long R_pad = (R + 255) / 256 * 256;
   for (long long r = R + threadIdx.x; r < R_pad; r += kScanThreads) row_map[r] = -1;
   if (threadIdx.x == 0) {
     sched->R = static_cast<int>(R);
