@@ -108,6 +108,20 @@ def recorded_traffic(kernel: str):
     return None
 
 
+def aggregate_ranks(ms: float, tokens: float, device) -> tuple[float, float]:
+    """Whole-job view of one timed region: the slowest rank's milliseconds and
+    the active tokens of all ranks (each rank processes its own batch)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms, tokens
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    n = torch.tensor([tokens], dtype=torch.float64, device=device)
+    dist.all_reduce(n, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(n.item())
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -314,11 +328,7 @@ def main():
             recs = eas.trace_read()
         barrier()
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms, _ = aggregate_ranks(e0.elapsed_time(e1), 0.0, dev)
         return ms / k, recs
 
     uuid = None
@@ -334,10 +344,7 @@ def main():
     clocks = sampler.stop() if sampler else None
     assert eas.read_device_status(ws) == 0 and eas.read_device_status(sws) == 0
 
-    tot_tokens = torch.tensor([float(Ta)], device=dev)
-    if world > 1:
-        dist.all_reduce(tot_tokens)
-    tokens_all = float(tot_tokens.item())
+    _, tokens_all = aggregate_ranks(0.0, float(Ta), dev)
     value = tokens_all / (ms / 1000.0)
     pk = peaks()
     flops_step = 8.0 * Ta * H * V

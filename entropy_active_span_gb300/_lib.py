@@ -38,6 +38,7 @@ SIGNATURES = {
                                       _P, _P, _P, _SZ, _P]),
     "eas_lmhead_fwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                               ctypes.c_int, _U32, _P, _P, _P, _P]),
+    "eas_selftest_wait_timeout": (ctypes.c_int, [_I64, _P, _SZ, _P]),
     "eas_read_device_status": (ctypes.c_int, [_P, _P]),
     "eas_trace_enable": (None, [_I32]),
     "eas_trace_read": (ctypes.c_int32, [_P, _P, _I32]),

@@ -637,6 +637,21 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
   return EAS_OK;
 }
 
+eas_status eas_selftest_wait_timeout(int64_t budget_cycles, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  if (budget_cycles < 1 || budget_cycles > (1LL << 34))
+    return fail(EAS_ERR_INVALID_ARG, "budget_cycles out of range");
+  if (!ws || ws_bytes < sizeof(DevStatus)) return fail(EAS_ERR_WORKSPACE, "workspace too small");
+  if (!aligned(ws, 16)) return fail(EAS_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  DevInfo di;
+  eas_status st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EAS_CUDA(cudaMemsetAsync(ws, 0, sizeof(DevStatus), s), "clear status");
+  EAS_CUDA(launch_selftest_wait(budget_cycles, static_cast<DevStatus*>(ws), s), "selftest");
+  return EAS_OK;
+}
+
 eas_status eas_read_device_status(const void* ws, void* stream) {
   if (!ws) return fail(EAS_ERR_INVALID_ARG, "null workspace");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

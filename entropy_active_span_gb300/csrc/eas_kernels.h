@@ -24,6 +24,7 @@ cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, co
                            cudaStream_t s);
 cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T,
                                       long long row_bytes, int num_sms, cudaStream_t s);
+cudaError_t launch_selftest_wait(long long budget, DevStatus* st, cudaStream_t s);
 
 // ---- tcgen05 GEMMs with fused epilogues, bf16 (eas_gemm_tc.cu) ----
 

@@ -413,3 +413,49 @@ cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T
 }
 
 }  // namespace eas
+
+namespace eas {
+
+// Failure-detection self-test: one warp waits on an mbarrier that nothing
+// arrives on, once with the CTA-scope wait and once with the cluster-scope
+// wait the GEMM kernel uses.  Each bounded wait runs out after `budget`
+// clocks and reports kStTimeout (where = 90 / 91) instead of hanging.
+__global__ void selftest_wait_kernel(long long budget, DevStatus* st) {
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar[0], 0, &abort_flag, budget)) report(st, kStTimeout, 90, 0);
+    abort_flag = 0;
+    long long t0 = clock64();
+    bool done = false;
+    while (!done && clock64() - t0 <= budget) {
+      uint32_t ok;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\t"
+          "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+          "selp.u32 %0, 1, 0, p;\n\t}"
+          : "=r"(ok)
+          : "r"(smem_u32(&bar[1])), "r"(0)
+          : "memory");
+      done = ok != 0;
+    }
+    if (!done) report(st, kStTimeout, 91, 0);
+    // complete both phases so that nothing is left pending at exit
+    mbar_arrive(&bar[0]);
+    mbar_arrive(&bar[1]);
+  }
+}
+
+cudaError_t launch_selftest_wait(long long budget, DevStatus* st, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(budget, st);
+  return cudaGetLastError();
+}
+
+}  // namespace eas

@@ -217,6 +217,18 @@ eas_status eas_lmhead_fwd_noalloc(const void* hidden, const void* weight,
 eas_status eas_read_device_status(const void* ws, void* stream);
 
 /*
+ * Failure-detection self-test.  Launches one warp that waits on a pipeline
+ * barrier nothing will complete, with the same bounded waits the GEMM kernels
+ * use, and lets each run out after budget_cycles SM clocks (1 .. 2^34).  Afterwards
+ * eas_read_device_status(ws) must report EAS_ERR_TIMEOUT and the device stays
+ * usable.  ws: at least 16 bytes (the status word).  The pipeline waits of the
+ * library kernels take their budget from the EAS_WAIT_BUDGET_CYCLES
+ * environment variable (default 2^31 clocks, about one second).
+ */
+eas_status eas_selftest_wait_timeout(int64_t budget_cycles, void* ws, size_t ws_bytes,
+                                     void* stream);
+
+/*
  * Per-kernel timing.  eas_trace_enable(1) clears earlier records and makes
  * every later kernel launch of this library record a pair of CUDA events
  * around itself on its stream; eas_trace_enable(0) stops recording.

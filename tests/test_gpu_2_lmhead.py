@@ -139,3 +139,30 @@ def test_active_rows_independent_of_row_policy():
     b = run_gpu(inp, flags=eas.EAS_ROWS_SPAN)
     for k in ("logprob", "entropy", "lse"):
         np.testing.assert_array_equal(a[k], b[k])
+
+
+@pytest.mark.parametrize("T,H,V", [(300, 192, 300), (513, 320, 1000), (1, 64, 50), (257, 448, 2049)])
+def test_bf16_hidden_width_not_a_tile_multiple(T, H, V):
+    """H % 256 != 0 leaves a partial N tile in dHidden and dW; T = 1 is a
+    single token; V just past a tile boundary leaves a one-column tail."""
+    inp = small_inputs(T, H, V, seed=T * 7 + H, mask_kind="bernoulli0.8", w_std=3.0)
+    if inp["mask"].sum() == 0:
+        inp["mask"][0] = 1
+    got = run_gpu(inp, vocab_chunk=512)
+    check(got, oracle_all(inp), inp["mask"], BF16_TOL)
+
+
+def test_autograd_wrapper_matches_oracle():
+    inp = small_inputs(700, 256, 900, seed=5, mask_kind="bernoulli0.6", w_std=3.0)
+    h = to_dev(inp["hidden"]).requires_grad_(True)
+    w = to_dev(inp["weight"]).requires_grad_(True)
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    lp, ent = eas.fused_logprob_entropy(h, w, t, m, vocab_chunk=256)
+    glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
+    (lp * glp + ent * gh).sum().backward()
+    ref = oracle_all(inp)
+    assert np.max(np.abs(lp.detach().cpu().numpy() - ref["logprob"])) <= BF16_TOL["lp"]
+    assert np.max(np.abs(ent.detach().cpu().numpy() - ref["entropy"])) <= BF16_TOL["ent"]
+    # the products lp*glp on inactive rows are 0 * g, so their gradients vanish there too
+    assert rel_fro(h.grad.float().cpu().numpy(), ref["dhidden"]) <= BF16_TOL["fro"]
+    assert rel_fro(w.grad.float().cpu().numpy(), ref["dweight"]) <= BF16_TOL["fro"]
