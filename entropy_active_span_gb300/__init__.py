@@ -22,7 +22,8 @@ __all__ = [
     "build_active_spans", "lmhead_fwd", "lmhead_bwd", "lmhead_workspace_size",
     "spans_workspace_size", "read_device_status", "workspace", "EasError",
     "EAS_ROWS_ACTIVE", "EAS_ROWS_SPAN", "EAS_DEFAULT_VOCAB_CHUNK", "FusedLMHeadLogprob",
-    "fused_logprob_entropy", "trace_enable", "trace_read",
+    "fused_logprob_entropy", "trace_enable", "trace_read", "lmhead_fwd_shard",
+    "lmhead_combine_shards", "lmhead_bwd_shard",
 ]
 
 
@@ -98,8 +99,11 @@ def build_active_spans(mask: torch.Tensor, max_gap: int = 128, cap: int | None =
 
 
 def lmhead_fwd(hidden, weight, targets, mask, spans, num_spans, flags: int = EAS_ROWS_ACTIVE,
-               ws=None, out=None):
-    """Target logprob, entropy and lse of the active rows.  Returns (logprob, entropy, lse)."""
+               ws=None, out=None, want_lse: bool = True):
+    """Target logprob, entropy and lse of the active rows.  Returns (logprob, entropy, lse).
+
+    With want_lse=False (forward-only scoring) lse is neither computed into
+    memory nor returned (None)."""
     dev = hidden.device
     dt = hidden.dtype
     code = _dtype_code(dt)
@@ -120,6 +124,8 @@ def lmhead_fwd(hidden, weight, targets, mask, spans, num_spans, flags: int = EAS
     if ws is None:
         ws = workspace(lmhead_workspace_size(T, H, V, dt), dev)
     logprob, entropy, lse = out
+    if not want_lse:
+        lse = None
     _lib.check(_lib.load().eas_lmhead_fwd(
         _ptr(hidden), _ptr(weight), _ptr(targets), _ptr(mask), _ptr(spans), _ptr(num_spans),
         int(spans.shape[0]), T, H, V, code, int(flags), _ptr(logprob), _ptr(entropy), _ptr(lse),
@@ -161,6 +167,74 @@ def lmhead_bwd(g_logprob, g_entropy, hidden, weight, targets, mask, spans, num_s
         T, H, V, code, int(flags), int(vocab_chunk), _ptr(dhidden), _ptr(dweight),
         _ptr(ws), ws.numel(), _stream(dev)))
     return dhidden, dweight
+
+
+def lmhead_fwd_shard(hidden, weight_shard, v_lo: int, targets, mask, spans, num_spans,
+                     flags: int = EAS_ROWS_ACTIVE, ws=None, stats=None):
+    """Per-token (M, S, U, z) statistics of one vocabulary shard ([T, 4] fp32)."""
+    dev = hidden.device
+    dt = hidden.dtype
+    T, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    for t, n, d in ((hidden, "hidden", dt), (weight_shard, "weight_shard", dt),
+                    (targets, "targets", torch.int32), (mask, "mask", torch.uint8),
+                    (spans, "spans", torch.int32), (num_spans, "num_spans", torch.int32)):
+        _need(t, n, d, dev)
+    if stats is None:
+        stats = torch.empty((T, 4), dtype=torch.float32, device=dev)
+    _need(stats, "stats", torch.float32, dev)
+    if ws is None:
+        ws = workspace(lmhead_workspace_size(T, H, Vs, dt), dev)
+    _lib.check(_lib.load().eas_lmhead_fwd_shard(
+        _ptr(hidden), _ptr(weight_shard), int(v_lo), _ptr(targets), _ptr(mask), _ptr(spans),
+        _ptr(num_spans), int(spans.shape[0]), T, H, Vs, _dtype_code(dt), int(flags),
+        _ptr(stats), _ptr(ws), ws.numel(), _stream(dev)))
+    return stats
+
+
+def lmhead_combine_shards(stats, mask, out=None, want_lse: bool = True):
+    """Merges [n_shards, T, 4] shard statistics into (logprob, entropy, lse)."""
+    dev = stats.device
+    n, T = int(stats.shape[0]), int(stats.shape[1])
+    _need(stats, "stats", torch.float32, dev)
+    _need(mask, "mask", torch.uint8, dev)
+    if out is None:
+        out = tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
+    lp, ent, lse = out
+    if not want_lse:
+        lse = None
+    _lib.check(_lib.load().eas_lmhead_combine_shards(_ptr(stats), n, T, _ptr(mask), _ptr(lp),
+                                                     _ptr(ent), _ptr(lse), _stream(dev)))
+    return lp, ent, lse
+
+
+def lmhead_bwd_shard(g_logprob, g_entropy, hidden, weight_shard, v_lo: int, targets, mask, spans,
+                     num_spans, lse, entropy, flags: int = EAS_ROWS_ACTIVE, vocab_chunk: int = 0,
+                     ws=None, dhidden_partial=None, dweight_shard=None):
+    """This shard's dW rows and partial dHidden (the partials sum to dHidden)."""
+    dev = hidden.device
+    dt = hidden.dtype
+    T, H = hidden.shape
+    Vs = weight_shard.shape[0]
+    for t, n in ((g_logprob, "g_logprob"), (g_entropy, "g_entropy"), (lse, "lse"),
+                 (entropy, "entropy")):
+        _need(t, n, torch.float32, dev)
+    for t, n, d in ((hidden, "hidden", dt), (weight_shard, "weight_shard", dt),
+                    (targets, "targets", torch.int32), (mask, "mask", torch.uint8),
+                    (spans, "spans", torch.int32), (num_spans, "num_spans", torch.int32)):
+        _need(t, n, d, dev)
+    if dhidden_partial is None:
+        dhidden_partial = torch.empty((T, H), dtype=dt, device=dev)
+    if dweight_shard is None:
+        dweight_shard = torch.empty((Vs, H), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(lmhead_workspace_size(T, H, Vs, dt, vocab_chunk), dev)
+    _lib.check(_lib.load().eas_lmhead_bwd_shard(
+        _ptr(g_logprob), _ptr(g_entropy), _ptr(hidden), _ptr(weight_shard), int(v_lo),
+        _ptr(targets), _ptr(mask), _ptr(spans), _ptr(num_spans), int(spans.shape[0]), _ptr(lse),
+        _ptr(entropy), T, H, Vs, _dtype_code(dt), int(flags), int(vocab_chunk),
+        _ptr(dhidden_partial), _ptr(dweight_shard), _ptr(ws), ws.numel(), _stream(dev)))
+    return dhidden_partial, dweight_shard
 
 
 def read_device_status(ws: torch.Tensor) -> int:
@@ -214,8 +288,14 @@ class FusedLMHeadLogprob(torch.autograd.Function):
 def fused_logprob_entropy(hidden, weight, targets, mask, spans=None, num_spans=None,
                           max_gap: int = 128, flags: int = EAS_ROWS_ACTIVE, vocab_chunk: int = 0):
     """Differentiable (logprob, entropy) of the active rows; builds the spans
-    from the mask on the device when they are not given."""
+    from the mask on the device when they are not given.  Under
+    torch.no_grad() (or when neither input needs a gradient) it runs the
+    forward alone and keeps no lse."""
     if spans is None or num_spans is None:
         spans, num_spans = build_active_spans(mask, max_gap)
+    if not (torch.is_grad_enabled() and (hidden.requires_grad or weight.requires_grad)):
+        lp, ent, _ = lmhead_fwd(hidden, weight, targets, mask, spans, num_spans, flags,
+                                want_lse=False)
+        return lp, ent
     return FusedLMHeadLogprob.apply(hidden, weight, targets, mask, spans, num_spans, flags,
                                     vocab_chunk)

@@ -36,6 +36,12 @@ SIGNATURES = {
     "eas_lmhead_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P,
                                       _I64, _I64, _I64, ctypes.c_int, _U32, _I64,
                                       _P, _P, _P, _SZ, _P]),
+    "eas_lmhead_fwd_shard": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                            ctypes.c_int, _U32, _P, _P, _SZ, _P]),
+    "eas_lmhead_combine_shards": (ctypes.c_int, [_P, _I32, _I64, _P, _P, _P, _P, _P]),
+    "eas_lmhead_bwd_shard": (ctypes.c_int, [_P, _P, _P, _P, _I64, _P, _P, _P, _P, _I64, _P, _P,
+                                            _I64, _I64, _I64, ctypes.c_int, _U32, _I64,
+                                            _P, _P, _P, _SZ, _P]),
     "eas_lmhead_fwd_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                               ctypes.c_int, _U32, _P, _P, _P, _P]),
     "eas_selftest_wait_timeout": (ctypes.c_int, [_I64, _P, _SZ, _P]),

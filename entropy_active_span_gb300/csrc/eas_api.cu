@@ -335,18 +335,23 @@ size_t eas_lmhead_workspace_size(int64_t T, int64_t H, int64_t V, eas_dtype dtyp
   return layout(T, H, V, dtype, vocab_chunk).total;
 }
 
-eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t* targets,
-                          const uint8_t* mask, const int32_t* spans, const int32_t* num_spans,
-                          int64_t cap, int64_t T, int64_t H, int64_t V, eas_dtype dtype,
-                          uint32_t flags, float* logprob, float* entropy, float* lse, void* ws,
-                          size_t ws_bytes, void* stream) {
+// Forward of the rows of `weight`, whose first row is vocabulary id t_off.
+// With stats == nullptr it writes the final logprob / entropy / lse (the whole
+// vocabulary); otherwise it writes each token's shard statistics to stats.
+static eas_status fwd_impl(const void* hidden, const void* weight, const int32_t* targets,
+                           const uint8_t* mask, const int32_t* spans, const int32_t* num_spans,
+                           int64_t cap, int64_t T, int64_t H, int64_t V, eas_dtype dtype,
+                           uint32_t flags, float* logprob, float* entropy, float* lse,
+                           float* stats, int64_t t_off, void* ws, size_t ws_bytes, void* stream) {
   eas_status st = check_shape(T, H, V, dtype);
   if (st != EAS_OK) return st;
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
   if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
   if (!weight || !num_spans || !ws) return fail(EAS_ERR_INVALID_ARG, "null pointer");
-  if (T > 0 && (!hidden || !targets || !mask || !logprob || !entropy || !lse || (cap > 0 && !spans)))
+  if (T > 0 && (!hidden || !targets || !mask || (cap > 0 && !spans)))
     return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (T > 0 && (stats ? !aligned(stats, 16) : (!logprob || !entropy)))
+    return fail(EAS_ERR_INVALID_ARG, "null or misaligned output");
   if (!aligned(hidden, 16) || !aligned(weight, 16) || !aligned(ws, 256))
     return fail(EAS_ERR_INVALID_ARG, "hidden/weight must be 16-byte and ws 256-byte aligned");
   const Layout L = layout(T, H, V, dtype, 0);
@@ -381,6 +386,7 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
     a.budget = wait_budget();
     a.row_map = at<int>(ws, L.row_map);
     a.targets = targets;
+    a.t_off = static_cast<int>(t_off);
     a.part_m = at<float>(ws, L.pm);
     a.part_s = at<float>(ws, L.ps);
     a.part_u = at<float>(ws, L.pu);
@@ -406,6 +412,7 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
     a.K_fixed = static_cast<int>(H);
     a.row_map = at<int>(ws, L.row_map);
     a.targets = targets;
+    a.t_off = static_cast<int>(t_off);
     a.part_m = at<float>(ws, L.pm);
     a.part_s = at<float>(ws, L.ps);
     a.part_u = at<float>(ws, L.pu);
@@ -420,20 +427,70 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
   }
   {
     Trace tr_(kTrCombine, s);
-    EAS_CUDA(launch_combine(at<float>(ws, L.pm), at<float>(ws, L.ps), at<float>(ws, L.pu),
-                            at<float>(ws, L.zt), L.n_vt, L.T_pad, at<int>(ws, L.pack_of), mask, T,
-                            logprob, entropy, lse, di.sms, s),
-             "combine");
+    if (stats) {
+      EAS_CUDA(launch_combine_stats(at<float>(ws, L.pm), at<float>(ws, L.ps), at<float>(ws, L.pu),
+                                    at<float>(ws, L.zt), L.n_vt, L.T_pad, at<int>(ws, L.pack_of),
+                                    mask, targets, static_cast<int>(t_off), static_cast<int>(V), T,
+                                    reinterpret_cast<float4*>(stats), di.sms, s),
+               "combine stats");
+    } else {
+      EAS_CUDA(launch_combine(at<float>(ws, L.pm), at<float>(ws, L.ps), at<float>(ws, L.pu),
+                              at<float>(ws, L.zt), L.n_vt, L.T_pad, at<int>(ws, L.pack_of), mask, T,
+                              logprob, entropy, lse, di.sms, s),
+               "combine");
+    }
   }
   return EAS_OK;
 }
 
-eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const void* hidden,
-                          const void* weight, const int32_t* targets, const uint8_t* mask,
-                          const int32_t* spans, const int32_t* num_spans, int64_t cap,
-                          const float* lse, const float* entropy, int64_t T, int64_t H, int64_t V,
-                          eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
-                          float* dweight, void* ws, size_t ws_bytes, void* stream) {
+eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t* targets,
+                          const uint8_t* mask, const int32_t* spans, const int32_t* num_spans,
+                          int64_t cap, int64_t T, int64_t H, int64_t V, eas_dtype dtype,
+                          uint32_t flags, float* logprob, float* entropy, float* lse, void* ws,
+                          size_t ws_bytes, void* stream) {
+  return fwd_impl(hidden, weight, targets, mask, spans, num_spans, cap, T, H, V, dtype, flags,
+                  logprob, entropy, lse, nullptr, 0, ws, ws_bytes, stream);
+}
+
+eas_status eas_lmhead_fwd_shard(const void* hidden, const void* weight_shard, int64_t v_lo,
+                                const int32_t* targets, const uint8_t* mask, const int32_t* spans,
+                                const int32_t* num_spans, int64_t cap, int64_t T, int64_t H,
+                                int64_t V_shard, eas_dtype dtype, uint32_t flags, float* stats,
+                                void* ws, size_t ws_bytes, void* stream) {
+  if (v_lo < 0 || v_lo > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "v_lo out of range");
+  if (T > 0 && !stats) return fail(EAS_ERR_INVALID_ARG, "null stats");
+  return fwd_impl(hidden, weight_shard, targets, mask, spans, num_spans, cap, T, H, V_shard, dtype,
+                  flags, nullptr, nullptr, nullptr, stats, v_lo, ws, ws_bytes, stream);
+}
+
+eas_status eas_lmhead_combine_shards(const float* stats, int32_t n_shards, int64_t T,
+                                     const uint8_t* mask, float* logprob, float* entropy,
+                                     float* lse, void* stream) {
+  if (n_shards < 1) return fail(EAS_ERR_INVALID_ARG, "n_shards must be >= 1");
+  if (T < 0 || T > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "T out of range");
+  if (T > 0 && (!stats || !mask || !logprob || !entropy))
+    return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (T > 0 && !aligned(stats, 16)) return fail(EAS_ERR_INVALID_ARG, "stats not 16-byte aligned");
+  DevInfo di;
+  eas_status st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Trace tr_(kTrCombine, s);
+  EAS_CUDA(launch_combine_shards(reinterpret_cast<const float4*>(stats), n_shards, T, mask,
+                                 logprob, entropy, lse, di.sms, s),
+           "combine shards");
+  return EAS_OK;
+}
+
+// Backward through the rows of `weight`, whose first row is vocabulary id
+// t_off (0 for the whole vocabulary).
+static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const void* hidden,
+                           const void* weight, const int32_t* targets, const uint8_t* mask,
+                           const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                           const float* lse, const float* entropy, int64_t T, int64_t H, int64_t V,
+                           eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
+                           float* dweight, int64_t t_off, void* ws, size_t ws_bytes,
+                           void* stream) {
   eas_status st = check_shape(T, H, V, dtype);
   if (st != EAS_OK) return st;
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
@@ -489,6 +546,7 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
     base.budget = wait_budget();
     base.row_map = at<int>(ws, L.row_map);
     base.targets = targets;
+    base.t_off = static_cast<int>(t_off);
     base.mask = mask;
     base.lse = lse;
     base.ent = entropy;
@@ -570,6 +628,7 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
     base.sched = sched;
     base.row_map = at<int>(ws, L.row_map);
     base.targets = targets;
+    base.t_off = static_cast<int>(t_off);
     base.mask = mask;
     base.lse = lse;
     base.ent = entropy;
@@ -635,6 +694,31 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
     }
   }
   return EAS_OK;
+}
+
+eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const void* hidden,
+                          const void* weight, const int32_t* targets, const uint8_t* mask,
+                          const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                          const float* lse, const float* entropy, int64_t T, int64_t H, int64_t V,
+                          eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
+                          float* dweight, void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(g_logprob, g_entropy, hidden, weight, targets, mask, spans, num_spans, cap, lse,
+                  entropy, T, H, V, dtype, flags, vocab_chunk, dhidden, dweight, 0, ws, ws_bytes,
+                  stream);
+}
+
+eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
+                                const void* hidden, const void* weight_shard, int64_t v_lo,
+                                const int32_t* targets, const uint8_t* mask, const int32_t* spans,
+                                const int32_t* num_spans, int64_t cap, const float* lse,
+                                const float* entropy, int64_t T, int64_t H, int64_t V_shard,
+                                eas_dtype dtype, uint32_t flags, int64_t vocab_chunk,
+                                void* dhidden_partial, float* dweight_shard, void* ws,
+                                size_t ws_bytes, void* stream) {
+  if (v_lo < 0 || v_lo > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "v_lo out of range");
+  return bwd_impl(g_logprob, g_entropy, hidden, weight_shard, targets, mask, spans, num_spans, cap,
+                  lse, entropy, T, H, V_shard, dtype, flags, vocab_chunk, dhidden_partial,
+                  dweight_shard, v_lo, ws, ws_bytes, stream);
 }
 
 eas_status eas_selftest_wait_timeout(int64_t budget_cycles, void* ws, size_t ws_bytes,

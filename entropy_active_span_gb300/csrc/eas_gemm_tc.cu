@@ -110,7 +110,7 @@ __device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_
     }
     const int cvalid = valid - c * 32;   // > 0
     const int tj = tgt - (n0 + c * 32);
-    if (static_cast<unsigned>(tj) < 32u) {
+    if (static_cast<unsigned>(tj) < static_cast<unsigned>(cvalid < 32 ? cvalid : 32)) {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (j == tj) ztv = v[j];
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       rs.active = false;
       bool active = false;
       if (kind == kTcFwd) {
-        if (tok >= 0) tgt = a.targets[tok];
+        if (tok >= 0) tgt = a.targets[tok] - a.t_off;
       } else if (kind == kTcDLogits) {
         active = (tok >= 0) && (a.mask[tok] != 0);
         rs.active = active;
@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
           rs.gh2 = gh * kLn2;
           rs.c1 = fmaf(gh, h, gl);
           rs.glp = gl;
-          const int tg = a.targets[tok] - jb.v0;
+          const int tg = a.targets[tok] - a.t_off - jb.v0;
           rs.tgt = (tg >= 0 && tg < jb.vc_live) ? tg : -1;
         }
       } else if (kind == kTcDHidden) {

@@ -22,6 +22,15 @@ cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, co
                            int n_tiles, long long stride, const int* pack_of, const uint8_t* mask,
                            long long T, float* logprob, float* entropy, float* lse, int num_sms,
                            cudaStream_t s);
+// Per-token statistics of one vocabulary shard instead of final outputs:
+// stats[t] = (M, S, U, z_target if the target lies in the shard else 0).
+cudaError_t launch_combine_stats(const float* pm, const float* ps, const float* pu,
+                                 const float* zt, int n_tiles, long long stride, const int* pack_of,
+                                 const uint8_t* mask, const int* targets, int t_off, int v_shard,
+                                 long long T, float4* stats, int num_sms, cudaStream_t s);
+cudaError_t launch_combine_shards(const float4* stats, int n_shards, long long T,
+                                  const uint8_t* mask, float* logprob, float* entropy, float* lse,
+                                  int num_sms, cudaStream_t s);
 cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T,
                                       long long row_bytes, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait(long long budget, DevStatus* st, cudaStream_t s);
@@ -72,6 +81,7 @@ struct TcArgs {
   // epilogue operands shared by the jobs
   const int* row_map;     // packed row -> token (or -1)
   const int* targets;     // [T]
+  int t_off;              // first vocabulary id of W's rows (vocabulary shard), else 0
   const uint8_t* mask;    // [T]
   const float* lse;       // [T]
   const float* ent;       // [T]
@@ -109,6 +119,7 @@ struct SimtArgs {
   int v0;
   const int* row_map;
   const int* targets;
+  int t_off;
   const uint8_t* mask;
   const float* lse;
   const float* ent;

@@ -338,18 +338,93 @@ combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
       if (r < 0) {
         logprob[t] = 0.f;
         entropy[t] = 0.f;
-        lse[t] = 0.f;
+        if (lse) lse[t] = 0.f;
       } else {
         Lse3 acc = st[0][x];
         for (int k = 1; k < kCombGroups; ++k) lse_merge(acc, st[k][x].m, st[k][x].s, st[k][x].u);
         const float logS = logf(acc.s);
         const float l = fmaf(acc.m, kLn2, logS);
-        lse[t] = l;
+        if (lse) lse[t] = l;
         entropy[t] = logS - (acc.u / acc.s) * kLn2;
         logprob[t] = zt[r] - l;
       }
     }
     __syncthreads();
+  }
+}
+
+// Vocabulary-parallel forward, shard side: the same fold as combine_kernel,
+// stopped before the logarithm.  stats[t] = (M, S, U, z_t) in base-2 units
+// over this shard's columns, z_t the target logit when the target lies in the
+// shard (else 0).  Inactive or unscheduled tokens get (0, 0, 0, 0).
+__global__ void __launch_bounds__(kCombTok * kCombGroups)
+combine_stats_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
+                     const float* __restrict__ pu, const float* __restrict__ zt, int n_tiles,
+                     long long stride, const int* __restrict__ pack_of,
+                     const uint8_t* __restrict__ mask, const int* __restrict__ targets, int t_off,
+                     int v_shard, long long T, float4* __restrict__ stats) {
+  __shared__ Lse3 st[kCombGroups][kCombTok];
+  const int x = threadIdx.x % kCombTok, g = threadIdx.x / kCombTok;
+  for (long long t0 = static_cast<long long>(blockIdx.x) * kCombTok; t0 < T;
+       t0 += static_cast<long long>(gridDim.x) * kCombTok) {
+    const long long t = t0 + x;
+    int r = -1;
+    if (t < T) {
+      r = pack_of[t];
+      if (r >= 0 && mask[t] == 0) r = -1;
+    }
+    Lse3 a{0.f, 0.f, 0.f};
+    if (r >= 0) {
+      for (int n = g; n < n_tiles; n += kCombGroups) {
+        const long long o = n * stride + r;
+        lse_merge(a, pm[o], ps[o], pu[o]);
+      }
+    }
+    st[g][x] = a;
+    __syncthreads();
+    if (g == 0 && t < T) {
+      if (r < 0) {
+        stats[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        Lse3 acc = st[0][x];
+        for (int k = 1; k < kCombGroups; ++k) lse_merge(acc, st[k][x].m, st[k][x].s, st[k][x].u);
+        const int tl = targets[t] - t_off;
+        const float z = (tl >= 0 && tl < v_shard) ? zt[r] : 0.f;
+        stats[t] = make_float4(acc.m, acc.s, acc.u, z);
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Vocabulary-parallel forward, gather side: merges the statistics of
+// n_shards shards in shard order (stats is [n_shards][T]) and finishes
+// lse = M ln2 + log S, H = log S - (U / S) ln2, logp = z_t - lse, with z_t
+// the sum of the shards' z slots (only the owning shard's is nonzero).
+__global__ void __launch_bounds__(256)
+combine_shards_kernel(const float4* __restrict__ stats, int n_shards, long long T,
+                      const uint8_t* __restrict__ mask, float* __restrict__ logprob,
+                      float* __restrict__ entropy, float* __restrict__ lse) {
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < T;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    if (mask[t] == 0) {
+      logprob[t] = 0.f;
+      entropy[t] = 0.f;
+      if (lse) lse[t] = 0.f;
+      continue;
+    }
+    Lse3 acc{0.f, 0.f, 0.f};
+    float z = 0.f;
+    for (int k = 0; k < n_shards; ++k) {
+      const float4 v = stats[static_cast<long long>(k) * T + t];
+      lse_merge(acc, v.x, v.y, v.z);
+      z += v.w;
+    }
+    const float logS = logf(acc.s);
+    const float l = fmaf(acc.m, kLn2, logS);
+    if (lse) lse[t] = l;
+    entropy[t] = logS - (acc.u / acc.s) * kLn2;
+    logprob[t] = z - l;
   }
 }
 
@@ -400,6 +475,29 @@ cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, co
   combine_kernel<<<static_cast<unsigned>(grid), kCombTok * kCombGroups, 0, s>>>(pm, ps, pu, zt, n_tiles, stride,
                                                              pack_of, mask, T, logprob, entropy,
                                                              lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_stats(const float* pm, const float* ps, const float* pu,
+                                 const float* zt, int n_tiles, long long stride, const int* pack_of,
+                                 const uint8_t* mask, const int* targets, int t_off, int v_shard,
+                                 long long T, float4* stats, int num_sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  long long grid = (T + kCombTok - 1) / kCombTok;
+  if (grid > 32LL * num_sms) grid = 32LL * num_sms;
+  combine_stats_kernel<<<static_cast<unsigned>(grid), kCombTok * kCombGroups, 0, s>>>(
+      pm, ps, pu, zt, n_tiles, stride, pack_of, mask, targets, t_off, v_shard, T, stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_shards(const float4* stats, int n_shards, long long T,
+                                  const uint8_t* mask, float* logprob, float* entropy, float* lse,
+                                  int num_sms, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  long long grid = (T + 255) / 256;
+  if (grid > 16LL * num_sms) grid = 16LL * num_sms;
+  combine_shards_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(stats, n_shards, T, mask,
+                                                                    logprob, entropy, lse);
   return cudaGetLastError();
 }
 

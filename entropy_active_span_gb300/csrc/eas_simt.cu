@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
       if (a.kind == kTcFwd) {
         // row statistics over this tile's valid columns (base-2 units)
         const int tok = mrow ? a.row_map[m] : -1;
-        const int tgt = (tok >= 0) ? a.targets[tok] : -1;
+        const int tgt = (tok >= 0) ? a.targets[tok] - a.t_off : -1;
         float mx = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs a) {
           h = a.ent[tok];
           gl = a.g_lp[tok];
           gh = a.g_h[tok];
-          tg = a.targets[tok] - a.v0;
+          tg = a.targets[tok] - a.t_off - a.v0;
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {

@@ -131,6 +131,8 @@ size_t eas_lmhead_workspace_size(int64_t T, int64_t H, int64_t V, eas_dtype dtyp
  *            EAS_ERR_INVALID_SPANS and all outputs are zero.
  *   flags    EAS_ROWS_ACTIVE or EAS_ROWS_SPAN
  *   logprob, entropy, lse  [T] fp32 out, overwritten; 0 on inactive rows.
+ *            lse may be NULL when no backward follows (forward-only scoring,
+ *            e.g. rollout log-probabilities and entropies).
  * Requirements: H % 64 == 0 (bf16) or H % 4 == 0 (fp32); V >= 1; T >= 0.
  */
 eas_status eas_lmhead_fwd(const void* hidden, const void* weight,
@@ -166,6 +168,50 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy,
                           int64_t vocab_chunk,
                           void* dhidden, float* dweight,
                           void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------ vocabulary-parallel path */
+
+/*
+ * Vocabulary-parallel (tensor-parallel) use, as in the page's TP4 matrix
+ * ("Performance"): W is split by rows into shards [v_lo, v_lo + V_shard),
+ * one per GPU, and every GPU holds the same hidden rows.
+ *
+ *   1. eas_lmhead_fwd_shard on each shard writes per-token statistics
+ *      stats[t] = (M, S, U, z) (4 floats, 16-byte aligned, [T][4]) over its
+ *      columns, in base-2 units (y = z log2 e):
+ *        M = max y, S = sum 2^(y - M), U = sum 2^(y - M) (y - M);
+ *      z is the target logit if the target lies in the shard, else 0;
+ *      inactive tokens get (0, 0, 0, 0).
+ *   2. The shards' statistics are gathered into [n_shards][T][4] (on several
+ *      GPUs: an all-gather), and eas_lmhead_combine_shards merges them in
+ *      shard order into logprob, entropy and lse (lse may be NULL).
+ *   3. eas_lmhead_bwd_shard on each shard, given the global lse and
+ *      entropy, writes that shard's dW rows [V_shard, H] and its partial
+ *      dHidden, i.e. its columns' contribution; the partials sum to dHidden
+ *      (on several GPUs: an all-reduce).
+ * Targets are global vocabulary ids.  Other arguments, workspaces and errors
+ * are those of eas_lmhead_fwd / eas_lmhead_bwd with V = V_shard.
+ */
+eas_status eas_lmhead_fwd_shard(const void* hidden, const void* weight_shard, int64_t v_lo,
+                                const int32_t* targets, const uint8_t* mask,
+                                const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                                int64_t T, int64_t H, int64_t V_shard, eas_dtype dtype,
+                                uint32_t flags, float* stats, void* ws, size_t ws_bytes,
+                                void* stream);
+
+eas_status eas_lmhead_combine_shards(const float* stats, int32_t n_shards, int64_t T,
+                                     const uint8_t* mask, float* logprob, float* entropy,
+                                     float* lse, void* stream);
+
+eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
+                                const void* hidden, const void* weight_shard, int64_t v_lo,
+                                const int32_t* targets, const uint8_t* mask,
+                                const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                                const float* lse, const float* entropy,
+                                int64_t T, int64_t H, int64_t V_shard, eas_dtype dtype,
+                                uint32_t flags, int64_t vocab_chunk,
+                                void* dhidden_partial, float* dweight_shard,
+                                void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------- allocation-free forward */
 

@@ -166,3 +166,61 @@ def test_autograd_wrapper_matches_oracle():
     # the products lp*glp on inactive rows are 0 * g, so their gradients vanish there too
     assert rel_fro(h.grad.float().cpu().numpy(), ref["dhidden"]) <= BF16_TOL["fro"]
     assert rel_fro(w.grad.float().cpu().numpy(), ref["dweight"]) <= BF16_TOL["fro"]
+
+
+def test_forward_only_scoring_matches_full_forward():
+    inp = small_inputs(900, 256, 1100, seed=9, mask_kind="bernoulli0.5", w_std=3.0)
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    spans, ns = eas.build_active_spans(m, 128)
+    lp, ent, lse = eas.lmhead_fwd(h, w, t, m, spans, ns)
+    lp2, ent2, lse2 = eas.lmhead_fwd(h, w, t, m, spans, ns, want_lse=False)
+    assert lse2 is None
+    assert torch.equal(lp, lp2) and torch.equal(ent, ent2)
+    with torch.no_grad():
+        lp3, ent3 = eas.fused_logprob_entropy(h, w, t, m)
+    assert torch.equal(lp, lp3) and torch.equal(ent, ent3)
+
+
+def test_step_captured_in_a_cuda_graph_matches_eager():
+    """spans + forward + backward enqueue only kernels and memsets on the
+    stream (no allocation, no host sync), so the whole step replays from a
+    CUDA graph with the same results."""
+    inp = small_inputs(1500, 256, 3000, seed=13, mask_kind="sparse_short", w_std=3.0)
+    T, H = inp["hidden"].shape
+    V = inp["weight"].shape[0]
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
+    spans = torch.empty((T, 2), dtype=torch.int32, device="cuda")
+    ns = torch.empty(1, dtype=torch.int32, device="cuda")
+    sws = eas.workspace(eas.spans_workspace_size(T), "cuda")
+    ws = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.bfloat16, 1024), "cuda")
+    lp, ent, lse = (torch.empty(T, device="cuda") for _ in range(3))
+    dh = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((V, H), dtype=torch.float32, device="cuda")
+
+    def step():
+        eas.build_active_spans(m, 128, spans=spans, num_spans=ns, ws=sws)
+        eas.lmhead_fwd(h, w, t, m, spans, ns, ws=ws, out=(lp, ent, lse))
+        eas.lmhead_bwd(glp, gh, h, w, t, m, spans, ns, lse, ent, vocab_chunk=1024, ws=ws,
+                       dhidden=dh, dweight=dw)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()                                   # eager, also warms up the launch paths
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    eager = [x.clone() for x in (lp, ent, lse, dh, dw)]
+    for x in (lp, ent, lse, dh, dw):
+        x.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert eas.read_device_status(ws) == 0
+    for a, b in zip(eager, (lp, ent, lse, dh, dw)):
+        assert torch.equal(a, b)
