@@ -22,7 +22,7 @@
 //
 // Tiles are 256 x 256 and computed by a cluster of two CTAs (the two SMs of a
 // TPC) with tcgen05.mma.cta_group::2: CTA r loads A rows [128r, 128r+128) and
-// B columns [128r, 128r+128) of the tile (32 KB per k-step of 64, six stages),
+// B columns [128r, 128r+128) of the tile (32 KB per k-step of 64, seven stages),
 // and each CTA's TMEM receives its 128 x 256 half of the accumulator.  CTA
 // layout (192 threads): warp 0 = TMA producer (lane 0; on the even CTA it also
 // fetches tile indices and publishes them to both CTAs), warp 1 = MMA issuer
@@ -300,7 +300,8 @@ __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, ui
 
 // =====================================================================
 // The CTA-pair kernel.  Against one CTA per 128 x 256 tile, the pair halves
-// the B bytes each SM moves from L2 and reads from shared memory per k-step.
+// the B bytes each SM moves from L2 and reads from shared memory per k-step,
+// and 32 KB stages allow seven of them (224 KB of the 227 KB per CTA).
 //
 // Synchronisation (each line: barrier, where it lives, who arrives):
 //   full[s]   leader   leader producer's expect_tx (64 KB) + both CTAs' TMA bytes
@@ -312,7 +313,7 @@ __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, ui
 //                      + 4 peer epilogue warps
 // =====================================================================
 
-constexpr int kPStages = 6;
+constexpr int kPStages = 7;
 constexpr int kPHalf = 128;                       // rows (of A) / columns (of B) per CTA
 constexpr int kPM = 256;                          // rows of a pair tile
 constexpr int kPABytes = kPHalf * kTcBK * 2;      // 16 KB
