@@ -23,7 +23,7 @@ __all__ = [
     "spans_workspace_size", "read_device_status", "workspace", "EasError",
     "EAS_ROWS_ACTIVE", "EAS_ROWS_SPAN", "EAS_DEFAULT_VOCAB_CHUNK", "FusedLMHeadLogprob",
     "fused_logprob_entropy", "trace_enable", "trace_read", "lmhead_fwd_shard",
-    "lmhead_combine_shards", "lmhead_bwd_shard",
+    "lmhead_combine_shards", "lmhead_bwd_shard", "cp_local_layout",
 ]
 
 
@@ -96,6 +96,24 @@ def build_active_spans(mask: torch.Tensor, max_gap: int = 128, cap: int | None =
         _ptr(mask), T, int(max_gap), _ptr(spans), int(spans.shape[0]), _ptr(num_spans),
         _ptr(ws), ws.numel(), _stream(dev)))
     return spans, num_spans
+
+
+def cp_local_layout(mask, seg_offsets, cp_size: int, cp_rank: int, ws=None):
+    """(local_mask uint8 [T/cp], local_to_global int32 [T/cp]) of one CP rank
+    under the load-balanced split of every packed segment into 2*cp chunks."""
+    dev = mask.device
+    _need(mask, "mask", torch.uint8, dev)
+    _need(seg_offsets, "seg_offsets", torch.int32, dev)
+    T = mask.numel()
+    n_local = T // cp_size
+    local_mask = torch.empty(n_local, dtype=torch.uint8, device=dev)
+    l2g = torch.empty(n_local, dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(64, dev)
+    _lib.check(_lib.load().eas_cp_local_layout(
+        _ptr(mask), _ptr(seg_offsets), int(seg_offsets.numel() - 1), T, int(cp_size),
+        int(cp_rank), _ptr(local_mask), _ptr(l2g), _ptr(ws), ws.numel(), _stream(dev)))
+    return local_mask, l2g
 
 
 def lmhead_fwd(hidden, weight, targets, mask, spans, num_spans, flags: int = EAS_ROWS_ACTIVE,

@@ -15,6 +15,7 @@ EAS_ERR_WORKSPACE = 4
 EAS_ERR_CUDA = 5
 EAS_ERR_TIMEOUT = 6
 EAS_ERR_SPAN_CAPACITY = 7
+EAS_ERR_INVALID_LAYOUT = 8
 
 EAS_BF16 = 0
 EAS_FP32 = 1
@@ -30,6 +31,7 @@ _P, _I64, _I32, _U32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, cty
 SIGNATURES = {
     "eas_spans_workspace_size": (_SZ, [_I64]),
     "eas_build_active_spans": (ctypes.c_int, [_P, _I64, _I32, _P, _I64, _P, _P, _SZ, _P]),
+    "eas_cp_local_layout": (ctypes.c_int, [_P, _P, _I32, _I64, _I32, _I32, _P, _P, _P, _SZ, _P]),
     "eas_lmhead_workspace_size": (_SZ, [_I64, _I64, _I64, ctypes.c_int, _I64]),
     "eas_lmhead_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                       ctypes.c_int, _U32, _P, _P, _P, _P, _SZ, _P]),

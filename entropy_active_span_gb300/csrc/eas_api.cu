@@ -721,6 +721,31 @@ eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
                   dweight_shard, v_lo, ws, ws_bytes, stream);
 }
 
+eas_status eas_cp_local_layout(const uint8_t* mask, const int32_t* seg_offsets, int32_t n_segs,
+                               int64_t T, int32_t cp_size, int32_t cp_rank, uint8_t* local_mask,
+                               int32_t* local_to_global, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (T < 0 || T > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "T out of range");
+  if (cp_size < 1 || cp_rank < 0 || cp_rank >= cp_size)
+    return fail(EAS_ERR_INVALID_ARG, "cp_rank %d outside [0, cp_size=%d)", cp_rank, cp_size);
+  if (T % (2LL * cp_size) != 0)
+    return fail(EAS_ERR_INVALID_ARG, "T=%lld is not a multiple of 2*cp_size", (long long)T);
+  if (n_segs < 1) return fail(EAS_ERR_INVALID_ARG, "n_segs must be >= 1");
+  if (!seg_offsets || (T > 0 && (!mask || !local_mask || !local_to_global)))
+    return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  if (!ws || ws_bytes < sizeof(DevStatus)) return fail(EAS_ERR_WORKSPACE, "workspace too small");
+  if (!aligned(ws, 16)) return fail(EAS_ERR_INVALID_ARG, "workspace not 16-byte aligned");
+  DevInfo di;
+  eas_status st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EAS_CUDA(cudaMemsetAsync(ws, 0, sizeof(DevStatus), s), "clear status");
+  EAS_CUDA(launch_cp_local(mask, seg_offsets, n_segs, T, cp_size, cp_rank, local_mask,
+                           local_to_global, static_cast<DevStatus*>(ws), di.sms, s),
+           "cp layout");
+  return EAS_OK;
+}
+
 eas_status eas_selftest_wait_timeout(int64_t budget_cycles, void* ws, size_t ws_bytes,
                                      void* stream) {
   if (budget_cycles < 1 || budget_cycles > (1LL << 34))
@@ -784,6 +809,7 @@ const char* eas_status_string(eas_status s) {
     case EAS_ERR_CUDA: return "EAS_ERR_CUDA";
     case EAS_ERR_TIMEOUT: return "EAS_ERR_TIMEOUT";
     case EAS_ERR_SPAN_CAPACITY: return "EAS_ERR_SPAN_CAPACITY";
+    case EAS_ERR_INVALID_LAYOUT: return "EAS_ERR_INVALID_LAYOUT";
   }
   return "EAS_UNKNOWN";
 }

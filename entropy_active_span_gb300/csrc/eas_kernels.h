@@ -34,6 +34,9 @@ cudaError_t launch_combine_shards(const float4* stats, int n_shards, long long T
 cudaError_t launch_zero_unpacked_rows(void* out, const int* pack_of, long long T,
                                       long long row_bytes, int num_sms, cudaStream_t s);
 cudaError_t launch_selftest_wait(long long budget, DevStatus* st, cudaStream_t s);
+cudaError_t launch_cp_local(const uint8_t* mask, const int* offs, int n_segs, long long T, int cp,
+                            int rank, uint8_t* local_mask, int* l2g, DevStatus* st, int num_sms,
+                            cudaStream_t s);
 
 // ---- tcgen05 GEMMs with fused epilogues, bf16 (eas_gemm_tc.cu) ----
 

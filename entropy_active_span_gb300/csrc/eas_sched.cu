@@ -557,3 +557,61 @@ cudaError_t launch_selftest_wait(long long budget, DevStatus* st, cudaStream_t s
 }
 
 }  // namespace eas
+
+namespace eas {
+
+// Context-parallel token layout ("How it works": forward mask and spans come
+// from a CP-aware packed layout; diagram: "CP-local ordered spans").  Every
+// packed segment [offs[k], offs[k+1]) has a length that is a multiple of 2*cp
+// and is cut into 2*cp equal chunks; rank `rank` holds chunk `rank` then chunk
+// 2*cp-1-rank of each segment, segments in order.  For each local token i:
+//   l2g[i] = its global token index, local_mask[i] = mask[l2g[i]].
+// Offsets that are not a valid layout report kStInvalidLayout; every access
+// stays in bounds regardless.
+__global__ void __launch_bounds__(256)
+cp_local_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ offs, int n_segs,
+                long long T, int cp, int rank, uint8_t* __restrict__ local_mask,
+                int* __restrict__ l2g, DevStatus* st) {
+  const long long n_local = T / cp;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long tid = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  for (long long k = tid; k < n_segs; k += stride) {
+    const long long L = static_cast<long long>(offs[k + 1]) - offs[k];
+    if (L < 0 || L % (2LL * cp) != 0) report(st, kStInvalidLayout, 95, static_cast<int>(k));
+  }
+  if (tid == 0 && (offs[0] != 0 || static_cast<long long>(offs[n_segs]) != T))
+    report(st, kStInvalidLayout, 96, -1);
+  for (long long i = tid; i < n_local; i += stride) {
+    int lo = 0, hi = n_segs;              // largest k with offs[k] / cp <= i
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (static_cast<long long>(offs[mid]) / cp <= i) lo = mid; else hi = mid;
+    }
+    const long long s0 = offs[lo];
+    const long long c = (static_cast<long long>(offs[lo + 1]) - s0) / (2LL * cp);
+    const long long p = i - s0 / cp;
+    const long long g = (p < c) ? s0 + rank * c + p : s0 + (2LL * cp - 1 - rank) * c + (p - c);
+    if (g >= 0 && g < T) {
+      l2g[i] = static_cast<int>(g);
+      local_mask[i] = mask[g];
+    } else {
+      l2g[i] = -1;
+      local_mask[i] = 0;
+      report(st, kStInvalidLayout, 97, static_cast<int>(i));
+    }
+  }
+}
+
+cudaError_t launch_cp_local(const uint8_t* mask, const int* offs, int n_segs, long long T, int cp,
+                            int rank, uint8_t* local_mask, int* l2g, DevStatus* st, int num_sms,
+                            cudaStream_t s) {
+  const long long work = T / cp > n_segs ? T / cp : n_segs;
+  long long grid = (work + 255) / 256;
+  if (grid < 1) grid = 1;
+  if (grid > 8LL * num_sms) grid = 8LL * num_sms;
+  cp_local_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(mask, offs, n_segs, T, cp, rank,
+                                                              local_mask, l2g, st);
+  return cudaGetLastError();
+}
+
+}  // namespace eas

@@ -62,7 +62,8 @@ typedef enum {
     EAS_ERR_WORKSPACE = 4,      /* workspace missing or smaller than required */
     EAS_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed           */
     EAS_ERR_TIMEOUT = 6,        /* a kernel pipeline wait ran out of time      */
-    EAS_ERR_SPAN_CAPACITY = 7   /* more spans than the caller's buffer holds   */
+    EAS_ERR_SPAN_CAPACITY = 7,  /* more spans than the caller's buffer holds   */
+    EAS_ERR_INVALID_LAYOUT = 8  /* packed-segment offsets not a valid CP layout */
 } eas_status;
 
 typedef enum {
@@ -105,6 +106,24 @@ size_t eas_spans_workspace_size(int64_t T);
 eas_status eas_build_active_spans(const uint8_t* mask, int64_t T, int32_t max_gap,
                                   int32_t* spans, int64_t cap, int32_t* num_spans,
                                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Context-parallel local layout ("How it works": forward mask and spans come
+ * from a CP-aware packed layout; diagram: "CP-local ordered spans").  Packed
+ * segments are [seg_offsets[k], seg_offsets[k+1]) for k < n_segs
+ * (seg_offsets[0] = 0, seg_offsets[n_segs] = T, device int32), each a
+ * multiple of 2*cp_size long.  Load-balanced split: every segment is cut into
+ * 2*cp_size equal chunks and rank cp_rank holds chunk cp_rank followed by
+ * chunk 2*cp_size-1-cp_rank, segments in order.  Writes, for each of the
+ * rank's T/cp_size local tokens, its global index (local_to_global) and its
+ * mask byte (local_mask).  Run eas_build_active_spans on local_mask to get
+ * the rank's CP-local ordered spans.  Offsets that do not form such a layout
+ * set EAS_ERR_INVALID_LAYOUT in the status word of ws (>= 16 bytes).
+ */
+eas_status eas_cp_local_layout(const uint8_t* mask, const int32_t* seg_offsets, int32_t n_segs,
+                               int64_t T, int32_t cp_size, int32_t cp_rank,
+                               uint8_t* local_mask, int32_t* local_to_global,
+                               void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- LM head */
 

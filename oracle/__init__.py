@@ -10,11 +10,12 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The GPU library never calls it.
 """
 from .spans import active_spans, span_rows
+from .cp import cp_local_mask, cp_local_to_global
 from .lmhead import (lmhead_forward, lmhead_forward_rows, lmhead_dlogits_rows,
                      lmhead_backward, lmhead_backward_rows_weighted, loss_value)
 
 __all__ = [
-    "active_spans", "span_rows", "lmhead_forward", "lmhead_forward_rows",
+    "active_spans", "span_rows", "cp_local_mask", "cp_local_to_global", "lmhead_forward", "lmhead_forward_rows",
     "lmhead_dlogits_rows", "lmhead_backward", "lmhead_backward_rows_weighted",
     "loss_value",
 ]
