@@ -255,9 +255,11 @@ eas_status check_shape(long long T, long long H, long long V, eas_dtype dt) {
 
 // Common prologue of forward and backward: status clear, span validation and
 // row schedule, packed copy of hidden.
+// Active tokens' targets must lie in [t_lo, t_hi) (checked on the device).
 eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* spans,
                     const int32_t* num_spans, int64_t cap, long long T, long long H,
-                    eas_dtype dt, uint32_t flags, void* ws, const Layout& L, const DevInfo& di,
+                    eas_dtype dt, uint32_t flags, const int32_t* targets, long long t_lo,
+                    long long t_hi, void* ws, const Layout& L, const DevInfo& di,
                     cudaStream_t s) {
   {
     Trace tr_(kTrMemset, s);
@@ -267,6 +269,8 @@ eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* span
   {
     Trace tr_(kTrRowmap, s);
     EAS_CUDA(launch_rowmap(mask, spans, num_spans, cap, T, (flags & EAS_ROWS_SPAN) ? 1 : 0,
+                           targets, static_cast<int>(t_lo),
+                           static_cast<int>(t_hi < 0x7fffffffLL ? t_hi : 0x7fffffffLL),
                            at<int>(ws, L.row_map), at<int>(ws, L.pack_of), at<Sched>(ws, L.sched),
                            at<DevStatus>(ws, L.status), s),
              "rowmap");
@@ -361,7 +365,8 @@ static eas_status fwd_impl(const void* hidden, const void* weight, const int32_t
   if (st != EAS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, ws, L, di, s);
+  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, targets, 0,
+                stats ? 0x7fffffffLL : static_cast<long long>(V), ws, L, di, s);
   if (st != EAS_OK || T == 0) return st;
   const Sched* sched = at<Sched>(ws, L.sched);
   const long long num_m_max = L.T_pad / tc_tile_rows();
@@ -489,8 +494,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
                            const int32_t* spans, const int32_t* num_spans, int64_t cap,
                            const float* lse, const float* entropy, int64_t T, int64_t H, int64_t V,
                            eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
-                           float* dweight, int64_t t_off, void* ws, size_t ws_bytes,
-                           void* stream) {
+                           float* dweight, int64_t t_off, bool sharded, void* ws,
+                           size_t ws_bytes, void* stream) {
   eas_status st = check_shape(T, H, V, dtype);
   if (st != EAS_OK) return st;
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
@@ -510,7 +515,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
   if (st != EAS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, ws, L, di, s);
+  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, targets, 0,
+                sharded ? 0x7fffffffLL : static_cast<long long>(V), ws, L, di, s);
   if (st != EAS_OK) return st;
   if (T == 0) {
     {
@@ -703,8 +709,8 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
                           eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
                           float* dweight, void* ws, size_t ws_bytes, void* stream) {
   return bwd_impl(g_logprob, g_entropy, hidden, weight, targets, mask, spans, num_spans, cap, lse,
-                  entropy, T, H, V, dtype, flags, vocab_chunk, dhidden, dweight, 0, ws, ws_bytes,
-                  stream);
+                  entropy, T, H, V, dtype, flags, vocab_chunk, dhidden, dweight, 0, false, ws,
+                  ws_bytes, stream);
 }
 
 eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
@@ -718,7 +724,7 @@ eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
   if (v_lo < 0 || v_lo > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "v_lo out of range");
   return bwd_impl(g_logprob, g_entropy, hidden, weight_shard, targets, mask, spans, num_spans, cap,
                   lse, entropy, T, H, V_shard, dtype, flags, vocab_chunk, dhidden_partial,
-                  dweight_shard, v_lo, ws, ws_bytes, stream);
+                  dweight_shard, v_lo, true, ws, ws_bytes, stream);
 }
 
 eas_status eas_cp_local_layout(const uint8_t* mask, const int32_t* seg_offsets, int32_t n_segs,

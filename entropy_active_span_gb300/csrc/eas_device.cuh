@@ -16,6 +16,7 @@ namespace eas {
 // Status codes written by kernels (same values as eas_status in eas.h).
 enum : int {
   kStOk = 0,
+  kStInvalidArg = 1,
   kStInvalidSpans = 2,
   kStTimeout = 6,
   kStSpanCapacity = 7,

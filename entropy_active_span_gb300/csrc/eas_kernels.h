@@ -14,8 +14,9 @@ struct Sched;
 cudaError_t launch_spans_build(const uint8_t* mask, long long T, int max_gap, int* spans,
                                long long cap, int* num_spans, DevStatus* st, cudaStream_t s);
 cudaError_t launch_rowmap(const uint8_t* mask, const int* spans, const int* num_spans,
-                          long long cap, long long T, int span_rows, int* row_map, int* pack_of,
-                          Sched* sched, DevStatus* st, cudaStream_t s);
+                          long long cap, long long T, int span_rows, const int* targets, int t_lo,
+                          int t_hi, int* row_map, int* pack_of, Sched* sched, DevStatus* st,
+                          cudaStream_t s);
 cudaError_t launch_gather_rows(const void* src, void* dst, const int* row_map, const Sched* sched,
                                long long T_pad, long long row_bytes, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, const float* zt,

@@ -158,10 +158,13 @@ spans_build_kernel(const uint8_t* __restrict__ mask, long long T, int max_gap,
 // A row is listed when it lies in a span and (policy EAS_ROWS_SPAN, or the
 // token is active).  Spans must be sorted, disjoint, inside [0, T) and cover
 // every active token; otherwise nothing is listed (R = 0) and the status word
-// reads kStInvalidSpans.
+// reads kStInvalidSpans.  Active tokens whose target lies outside [t_lo, t_hi)
+// set kStInvalidArg (their outputs are then meaningless; nothing is read out
+// of bounds).
 __global__ void __launch_bounds__(kScanThreads)
 rowmap_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
               const int* __restrict__ num_spans, long long cap, long long T, int span_rows,
+              const int* __restrict__ targets, int t_lo, int t_hi,
               int* __restrict__ row_map, int* __restrict__ pack_of, Sched* sched,
               DevStatus* st) {
   __shared__ int sm_i[32];
@@ -208,6 +211,10 @@ rowmap_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
       const bool covered = (k >= 0) && (t < static_cast<long long>(spans[2 * k + 1]));
       const bool active = mask[t] != 0;
       if (active && !covered) uncovered = true;
+      if (active && targets != nullptr) {
+        const int tg = targets[t];
+        if (tg < t_lo || tg >= t_hi) report(st, kStInvalidArg, 3, static_cast<int>(t));
+      }
       if (covered && (span_rows || active)) {
         sel |= 1u << i;
         ++cnt;
@@ -449,10 +456,11 @@ cudaError_t launch_spans_build(const uint8_t* mask, long long T, int max_gap, in
 }
 
 cudaError_t launch_rowmap(const uint8_t* mask, const int* spans, const int* num_spans,
-                          long long cap, long long T, int span_rows, int* row_map, int* pack_of,
-                          Sched* sched, DevStatus* st, cudaStream_t s) {
-  rowmap_kernel<<<1, kScanThreads, 0, s>>>(mask, spans, num_spans, cap, T, span_rows, row_map,
-                                           pack_of, sched, st);
+                          long long cap, long long T, int span_rows, const int* targets, int t_lo,
+                          int t_hi, int* row_map, int* pack_of, Sched* sched, DevStatus* st,
+                          cudaStream_t s) {
+  rowmap_kernel<<<1, kScanThreads, 0, s>>>(mask, spans, num_spans, cap, T, span_rows, targets,
+                                           t_lo, t_hi, row_map, pack_of, sched, st);
   return cudaGetLastError();
 }
 

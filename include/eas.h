@@ -142,7 +142,9 @@ size_t eas_lmhead_workspace_size(int64_t T, int64_t H, int64_t V, eas_dtype dtyp
  *
  *   hidden   [T, H]  bf16 or fp32 (dtype)
  *   weight   [V, H]  same dtype
- *   targets  [T] int32, read only on active rows, must be in [0, V)
+ *   targets  [T] int32, read only on active rows, must be in [0, V); an
+ *            active row whose target is outside sets EAS_ERR_INVALID_ARG in
+ *            the status word (that row's outputs are then meaningless)
  *   mask     [T] uint8 loss mask
  *   spans, num_spans, cap : spans as produced by eas_build_active_spans (or
  *            by the caller); they must be sorted, disjoint, inside [0, T)

@@ -224,3 +224,22 @@ def test_step_captured_in_a_cuda_graph_matches_eager():
     assert eas.read_device_status(ws) == 0
     for a, b in zip(eager, (lp, ent, lse, dh, dw)):
         assert torch.equal(a, b)
+
+
+def test_out_of_range_target_is_reported():
+    inp = small_inputs(300, 128, 400, mask_kind="dense", w_std=2.0)
+    inp["targets"] = inp["targets"].copy()
+    inp["targets"][17] = 400                       # == V
+    got = run_gpu(inp, want_status=True)
+    assert got["status"] == (_lib.EAS_ERR_INVALID_ARG, _lib.EAS_ERR_INVALID_ARG)
+
+
+def test_very_large_logits_stay_finite_and_match():
+    """W std 60 gives logits of magnitude ~100: the online max keeps every
+    exponent in range and the forward and gradients still match the oracle
+    at the usual tolerances."""
+    inp = small_inputs(400, 256, 1500, seed=31, mask_kind="bernoulli0.7", w_std=60.0)
+    got = run_gpu(inp, vocab_chunk=512)
+    for k in got:
+        assert np.all(np.isfinite(got[k])), k
+    check(got, oracle_all(inp), inp["mask"], BF16_TOL)
