@@ -73,6 +73,7 @@ def parse_args():
     p.add_argument("--rows", choices=("active", "span"), default="active")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-dense", action="store_true")
+    p.add_argument("--no-forward-only", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample")
@@ -205,7 +206,8 @@ def reference_arm(args, rank):
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem,temperature.gpu")
 
     def __init__(self, uuid: str | None):
         self.proc = None
@@ -230,7 +232,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, mem, pw, temp = [], None, set(), [], [], []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
@@ -239,6 +241,10 @@ class ClockSampler:
             try:
                 sm.append(float(parts[0]))
                 mx = float(parts[1])
+                pw.append(float(parts[2]))
+                if len(parts) >= 10:
+                    mem.append(float(parts[8]))
+                    temp.append(float(parts[9]))
             except ValueError:
                 continue
             for name, v in zip(names, parts[4:8]):
@@ -247,8 +253,12 @@ class ClockSampler:
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(sm), "power_w_median": statistics.median(pw) if pw else None}
+        if mem:
+            out["mem_mhz"] = statistics.median(mem)
+            out["temp_c_max"] = max(temp)
+        return out
 
 
 # -------------------------------------------------------------- our arm
@@ -383,6 +393,39 @@ def main():
                  "tflops": 8.0 * T * H * V / (dms / 1000.0) / 1e12,
                  "frac_of_peak": 8.0 * T * H * V / (dms / 1000.0) / 1e12 / pk["bf16_sustained"]}
 
+    # ---- forward-only scoring (no lse kept): bf16 operands, and e4m3 operands
+    # with W quantised once and hidden quantised inside every step
+    fwd_only = None
+    if not args.no_forward_only:
+        ws_fwd = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.bfloat16), dev)
+
+        def score_bf16():
+            eas.build_active_spans(mask, args.max_gap, spans=spans, num_spans=ns, ws=sws)
+            eas.lmhead_fwd(hidden, weight, targets, mask, spans, ns, flags, ws=ws_fwd,
+                           out=(lp, ent, lse), want_lse=False)
+
+        w8, wsc = eas.quantize_rows_e4m3(weight)
+        h8 = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        hsc = torch.empty(T, dtype=torch.float32, device=dev)
+        ws8 = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.uint8), dev)
+
+        def score_fp8():
+            eas.quantize_rows_e4m3(hidden, out=h8, scale=hsc)
+            eas.build_active_spans(mask, args.max_gap, spans=spans, num_spans=ns, ws=sws)
+            eas.lmhead_fwd_fp8(h8, hsc, w8, wsc, targets, mask, spans, ns, flags, ws=ws8,
+                               out=(lp, ent, lse), want_lse=False)
+
+        fwd_only = {}
+        for name, fn, peak in (("bf16", score_bf16, pk["bf16_sustained"]),
+                               ("e4m3", score_fp8, 2.0 * pk["bf16_sustained"])):
+            fms, _ = timed(fn, args.steps)
+            tf = 2.0 * Ta * H * V / (fms / 1000.0) / 1e12
+            fwd_only[name] = {"ms_per_step": fms, "active_tokens_per_s": tokens_all / (fms / 1000.0),
+                              "tflops": tf, "peak_tflops": peak, "frac_of_peak": tf / peak}
+        fwd_only["e4m3"]["peak_kind"] = ("bf16_tflops_sustained x 2 (nominal dense fp8/bf16 "
+                                         "ratio 4.5/2.25)")
+        del ws_fwd, ws8, h8, w8
+
     # ---- end to end: host (pinned) inputs in, results out, through the API
     e2e = None
     if not args.no_e2e:
@@ -438,6 +481,7 @@ def main():
             "gemm_tflops": gemm_tflops,
             "gpu_launches": launches,
             "dense_ablation": dense,
+            "forward_only": fwd_only,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,

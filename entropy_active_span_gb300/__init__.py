@@ -15,7 +15,7 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (EAS_BF16, EAS_DEFAULT_VOCAB_CHUNK, EAS_FP32, EAS_ROWS_ACTIVE,
+from ._lib import (EAS_BF16, EAS_DEFAULT_VOCAB_CHUNK, EAS_E4M3, EAS_FP32, EAS_ROWS_ACTIVE,
                    EAS_ROWS_SPAN, EasError)
 
 __all__ = [
@@ -23,7 +23,8 @@ __all__ = [
     "spans_workspace_size", "read_device_status", "workspace", "EasError",
     "EAS_ROWS_ACTIVE", "EAS_ROWS_SPAN", "EAS_DEFAULT_VOCAB_CHUNK", "FusedLMHeadLogprob",
     "fused_logprob_entropy", "trace_enable", "trace_read", "lmhead_fwd_shard",
-    "lmhead_combine_shards", "lmhead_bwd_shard", "cp_local_layout",
+    "lmhead_combine_shards", "lmhead_bwd_shard", "cp_local_layout", "quantize_rows_e4m3",
+    "lmhead_fwd_fp8",
 ]
 
 
@@ -44,7 +45,13 @@ def _dtype_code(dt: torch.dtype) -> int:
         return EAS_BF16
     if dt == torch.float32:
         return EAS_FP32
-    raise TypeError(f"hidden/weight must be bfloat16 or float32, got {dt}")
+    if dt in (torch.uint8, torch.float8_e4m3fn):
+        return EAS_E4M3
+    raise TypeError(f"hidden/weight must be bfloat16, float32 or e4m3, got {dt}")
+
+
+def _as_codes(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t
 
 
 def _need(t: torch.Tensor, name: str, dtype: torch.dtype, device) -> None:
@@ -185,6 +192,52 @@ def lmhead_bwd(g_logprob, g_entropy, hidden, weight, targets, mask, spans, num_s
         T, H, V, code, int(flags), int(vocab_chunk), _ptr(dhidden), _ptr(dweight),
         _ptr(ws), ws.numel(), _stream(dev)))
     return dhidden, dweight
+
+
+def quantize_rows_e4m3(x: torch.Tensor, out=None, scale=None):
+    """Per-row e4m3 quantisation of a bf16/fp32 [R, H] tensor on the device.
+    Returns (codes uint8 [R, H], scale fp32 [R])."""
+    dev = x.device
+    code = _dtype_code(x.dtype)
+    if code == EAS_E4M3:
+        raise TypeError("x must be bfloat16 or float32")
+    _need(x, "x", x.dtype, dev)
+    R, H = x.shape
+    if out is None:
+        out = torch.empty((R, H), dtype=torch.uint8, device=dev)
+    if scale is None:
+        scale = torch.empty(R, dtype=torch.float32, device=dev)
+    _lib.check(_lib.load().eas_quantize_rows_e4m3(_ptr(x), code, R, H, _ptr(out), _ptr(scale),
+                                                  _stream(dev)))
+    return out, scale
+
+
+def lmhead_fwd_fp8(hidden_e4m3, hidden_scale, weight_e4m3, weight_scale, targets, mask, spans,
+                   num_spans, flags: int = EAS_ROWS_ACTIVE, ws=None, out=None,
+                   want_lse: bool = True):
+    """Forward with e4m3 operands and per-row scales (forward-only scoring)."""
+    h8, w8 = _as_codes(hidden_e4m3), _as_codes(weight_e4m3)
+    dev = h8.device
+    T, H = h8.shape
+    V = w8.shape[0]
+    for t, n, d in ((h8, "hidden_e4m3", torch.uint8), (w8, "weight_e4m3", torch.uint8),
+                    (hidden_scale, "hidden_scale", torch.float32),
+                    (weight_scale, "weight_scale", torch.float32),
+                    (targets, "targets", torch.int32), (mask, "mask", torch.uint8),
+                    (spans, "spans", torch.int32), (num_spans, "num_spans", torch.int32)):
+        _need(t, n, d, dev)
+    if out is None:
+        out = tuple(torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
+    lp, ent, lse = out
+    if not want_lse:
+        lse = None
+    if ws is None:
+        ws = workspace(lmhead_workspace_size(T, H, V, torch.uint8), dev)
+    _lib.check(_lib.load().eas_lmhead_fwd_fp8(
+        _ptr(h8), _ptr(hidden_scale), _ptr(w8), _ptr(weight_scale), _ptr(targets), _ptr(mask),
+        _ptr(spans), _ptr(num_spans), int(spans.shape[0]), T, H, V, int(flags), _ptr(lp),
+        _ptr(ent), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)))
+    return lp, ent, lse
 
 
 def lmhead_fwd_shard(hidden, weight_shard, v_lo: int, targets, mask, spans, num_spans,

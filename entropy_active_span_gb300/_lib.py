@@ -19,6 +19,7 @@ EAS_ERR_INVALID_LAYOUT = 8
 
 EAS_BF16 = 0
 EAS_FP32 = 1
+EAS_E4M3 = 2
 
 EAS_ROWS_ACTIVE = 0
 EAS_ROWS_SPAN = 1
@@ -38,6 +39,9 @@ SIGNATURES = {
     "eas_lmhead_bwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P,
                                       _I64, _I64, _I64, ctypes.c_int, _U32, _I64,
                                       _P, _P, _P, _SZ, _P]),
+    "eas_quantize_rows_e4m3": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _P, _P]),
+    "eas_lmhead_fwd_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                          _U32, _P, _P, _P, _P, _SZ, _P]),
     "eas_lmhead_fwd_shard": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                             ctypes.c_int, _U32, _P, _P, _SZ, _P]),
     "eas_lmhead_combine_shards": (ctypes.c_int, [_P, _I32, _I64, _P, _P, _P, _P, _P]),

@@ -163,18 +163,19 @@ eas_status get_encoder(EncodeTiledFn* fn) {
   return EAS_OK;
 }
 
-// 2-D bf16 tensor [rows][cols] with row pitch `ld` elements, 128-byte swizzle,
-// box of 64 columns x box_rows rows; out-of-range elements read as zero.
-eas_status make_map_bf16(CUtensorMap* m, const void* base, long long cols, long long rows,
-                         long long ld, int box_rows) {
+// 2-D tensor [rows][cols] with row pitch `ld` elements, 128-byte swizzle, box
+// of 128 bytes (64 bf16 or 128 one-byte elements) x box_rows rows;
+// out-of-range elements read as zero.
+eas_status make_map_2d(CUtensorMap* m, CUtensorMapDataType type, int esize, const void* base,
+                       long long cols, long long rows, long long ld, int box_rows) {
   EncodeTiledFn enc;
   eas_status s = get_encoder(&enc);
   if (s != EAS_OK) return s;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = enc(m, type, 2, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
@@ -182,6 +183,18 @@ eas_status make_map_bf16(CUtensorMap* m, const void* base, long long cols, long 
                 static_cast<int>(r), rows, cols, ld);
   return EAS_OK;
 }
+
+eas_status make_map_bf16(CUtensorMap* m, const void* base, long long cols, long long rows,
+                         long long ld, int box_rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, ld, box_rows);
+}
+
+eas_status make_map_u8(CUtensorMap* m, const void* base, long long cols, long long rows,
+                       long long ld, int box_rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, cols, rows, ld, box_rows);
+}
+
+size_t elem_size(eas_dtype dt) { return dt == EAS_BF16 ? 2 : dt == EAS_E4M3 ? 1 : 4; }
 
 // ---------------------------------------------------------- workspace layout
 
@@ -203,9 +216,9 @@ size_t align_up(size_t x) { return (x + 1023) / 1024 * 1024; }
 
 Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chunk) {
   Layout L;
-  const size_t esz = (dt == EAS_BF16) ? 2 : 4;
+  const size_t esz = elem_size(dt);
   L.T_pad = round_up(T, 256);
-  L.vt = (dt == EAS_BF16) ? kTcBN : kSimtBN;
+  L.vt = (dt == EAS_FP32) ? kSimtBN : kTcBN;
   L.n_vt = static_cast<int>(cdiv(V, L.vt));
   if (chunk <= 0) chunk = EAS_DEFAULT_VOCAB_CHUNK;
   L.vc = chunk < V ? chunk : V;
@@ -245,7 +258,10 @@ eas_status check_shape(long long T, long long H, long long V, eas_dtype dt) {
   if (T < 0 || T > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "T=%lld out of range", T);
   if (V < 1 || V > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "V=%lld out of range", V);
   if (H < 1 || H > (1LL << 20)) return fail(EAS_ERR_INVALID_ARG, "H=%lld out of range", H);
-  if (dt != EAS_BF16 && dt != EAS_FP32) return fail(EAS_ERR_INVALID_ARG, "dtype %d", (int)dt);
+  if (dt != EAS_BF16 && dt != EAS_FP32 && dt != EAS_E4M3)
+    return fail(EAS_ERR_INVALID_ARG, "dtype %d", (int)dt);
+  if (dt == EAS_E4M3 && H % 128 != 0)
+    return fail(EAS_ERR_UNSUPPORTED, "e4m3 path needs H %% 128 == 0 (H=%lld)", H);
   if (dt == EAS_BF16 && H % 64 != 0)
     return fail(EAS_ERR_UNSUPPORTED, "bf16 path needs H %% 64 == 0 (H=%lld)", H);
   if (dt == EAS_FP32 && H % 4 != 0)
@@ -275,7 +291,7 @@ eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* span
                            at<DevStatus>(ws, L.status), s),
              "rowmap");
   }
-  const long long row_bytes = H * ((dt == EAS_BF16) ? 2 : 4);
+  const long long row_bytes = H * static_cast<long long>(elem_size(dt));
   {
     Trace tr_(kTrGather, s);
     EAS_CUDA(launch_gather_rows(hidden, at<char>(ws, L.hp), at<int>(ws, L.row_map),
@@ -346,9 +362,13 @@ static eas_status fwd_impl(const void* hidden, const void* weight, const int32_t
                            const uint8_t* mask, const int32_t* spans, const int32_t* num_spans,
                            int64_t cap, int64_t T, int64_t H, int64_t V, eas_dtype dtype,
                            uint32_t flags, float* logprob, float* entropy, float* lse,
-                           float* stats, int64_t t_off, void* ws, size_t ws_bytes, void* stream) {
+                           float* stats, int64_t t_off, const float* hscale,
+                           const float* wscale, void* ws, size_t ws_bytes, void* stream) {
   eas_status st = check_shape(T, H, V, dtype);
   if (st != EAS_OK) return st;
+  if ((dtype == EAS_E4M3) != (hscale != nullptr && wscale != nullptr))
+    return fail(EAS_ERR_INVALID_ARG,
+                "e4m3 operands are taken (with their scales) by eas_lmhead_fwd_fp8 only");
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
   if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
   if (!weight || !num_spans || !ws) return fail(EAS_ERR_INVALID_ARG, "null pointer");
@@ -371,19 +391,24 @@ static eas_status fwd_impl(const void* hidden, const void* weight, const int32_t
   const Sched* sched = at<Sched>(ws, L.sched);
   const long long num_m_max = L.T_pad / tc_tile_rows();
 
-  if (dtype == EAS_BF16) {
+  if (dtype == EAS_BF16 || dtype == EAS_E4M3) {
+    const bool fp8 = (dtype == EAS_E4M3);
     TcArgs a;
     memset(&a, 0, sizeof(a));
     TcJob& j = a.jobs[0];
-    st = make_map_bf16(&j.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128);
+    st = fp8 ? make_map_u8(&j.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128)
+             : make_map_bf16(&j.tmA, at<char>(ws, L.hp), H, L.T_pad, H, 128);
     if (st != EAS_OK) return st;
-    st = make_map_bf16(&j.tmB, weight, H, V, H, tc_tile_rows() == 256 ? 128 : 256);
+    st = fp8 ? make_map_u8(&j.tmB, weight, H, V, H, 128)
+             : make_map_bf16(&j.tmB, weight, H, V, H, tc_tile_rows() == 256 ? 128 : 256);
     if (st != EAS_OK) return st;
-    j.kind = kTcFwd;
+    j.kind = fp8 ? kTcFwdFp8 : kTcFwd;
+    a.hscale = hscale;
+    a.wscale = wscale;
     j.M_fixed = 0;
     j.N = static_cast<int>(V);
     j.K_fixed = static_cast<int>(H);
-    j.group_m = group_for(tc_tile_rows() * H * 2LL, num_m_max);
+    j.group_m = group_for(tc_tile_rows() * H * static_cast<long long>(elem_size(dtype)), num_m_max);
     a.n_jobs = 1;
     a.sched = sched;
     a.status = at<DevStatus>(ws, L.status);
@@ -454,7 +479,34 @@ eas_status eas_lmhead_fwd(const void* hidden, const void* weight, const int32_t*
                           uint32_t flags, float* logprob, float* entropy, float* lse, void* ws,
                           size_t ws_bytes, void* stream) {
   return fwd_impl(hidden, weight, targets, mask, spans, num_spans, cap, T, H, V, dtype, flags,
-                  logprob, entropy, lse, nullptr, 0, ws, ws_bytes, stream);
+                  logprob, entropy, lse, nullptr, 0, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+eas_status eas_lmhead_fwd_fp8(const uint8_t* hidden_e4m3, const float* hidden_scale,
+                              const uint8_t* weight_e4m3, const float* weight_scale,
+                              const int32_t* targets, const uint8_t* mask, const int32_t* spans,
+                              const int32_t* num_spans, int64_t cap, int64_t T, int64_t H,
+                              int64_t V, uint32_t flags, float* logprob, float* entropy,
+                              float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (!weight_scale || (T > 0 && !hidden_scale)) return fail(EAS_ERR_INVALID_ARG, "null scale");
+  return fwd_impl(hidden_e4m3, weight_e4m3, targets, mask, spans, num_spans, cap, T, H, V,
+                  EAS_E4M3, flags, logprob, entropy, lse, nullptr, 0,
+                  hidden_scale ? hidden_scale : weight_scale, weight_scale, ws, ws_bytes, stream);
+}
+
+eas_status eas_quantize_rows_e4m3(const void* src, eas_dtype src_dtype, int64_t R, int64_t H,
+                                  uint8_t* dst, float* scale, void* stream) {
+  if (src_dtype != EAS_BF16 && src_dtype != EAS_FP32)
+    return fail(EAS_ERR_INVALID_ARG, "source must be bf16 or fp32");
+  if (R < 0 || H < 1) return fail(EAS_ERR_INVALID_ARG, "bad shape");
+  if (R > 0 && (!src || !dst || !scale)) return fail(EAS_ERR_INVALID_ARG, "null pointer");
+  DevInfo di;
+  eas_status st = device_info(&di);
+  if (st != EAS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EAS_CUDA(launch_quantize_rows_e4m3(src, src_dtype == EAS_BF16, R, H, dst, scale, di.sms, s),
+           "quantize");
+  return EAS_OK;
 }
 
 eas_status eas_lmhead_fwd_shard(const void* hidden, const void* weight_shard, int64_t v_lo,
@@ -465,7 +517,8 @@ eas_status eas_lmhead_fwd_shard(const void* hidden, const void* weight_shard, in
   if (v_lo < 0 || v_lo > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "v_lo out of range");
   if (T > 0 && !stats) return fail(EAS_ERR_INVALID_ARG, "null stats");
   return fwd_impl(hidden, weight_shard, targets, mask, spans, num_spans, cap, T, H, V_shard, dtype,
-                  flags, nullptr, nullptr, nullptr, stats, v_lo, ws, ws_bytes, stream);
+                  flags, nullptr, nullptr, nullptr, stats, v_lo, nullptr, nullptr, ws, ws_bytes,
+                  stream);
 }
 
 eas_status eas_lmhead_combine_shards(const float* stats, int32_t n_shards, int64_t T,
@@ -498,6 +551,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
                            size_t ws_bytes, void* stream) {
   eas_status st = check_shape(T, H, V, dtype);
   if (st != EAS_OK) return st;
+  if (dtype == EAS_E4M3)
+    return fail(EAS_ERR_UNSUPPORTED, "the backward takes bf16 or fp32 operands");
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
   if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
   if (vocab_chunk < 0) return fail(EAS_ERR_INVALID_ARG, "vocab_chunk must be >= 0");

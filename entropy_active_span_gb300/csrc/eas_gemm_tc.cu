@@ -90,8 +90,10 @@ __device__ __forceinline__ Work locate(int t, const JobShape (&js)[kMaxTcJobs], 
 // Forward: per-row online softmax statistics over the tile's valid columns,
 // in base-2 units (y = z log2 e): m = max y, s = sum 2^(y-m), u = sum
 // 2^(y-m)(y-m); plus the target logit when the target falls in this tile.
+template <bool kScaled>
 __device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_empty,
-                                        long long r0, int n_blk, int row, int tgt) {
+                                        long long r0, int n_blk, int row, int tgt,
+                                        float rscale, const float* __restrict__ wscale) {
   const int n0 = n_blk * kTcBN;
   int valid = a.V - n0;
   if (valid > kTcBN) valid = kTcBN;
@@ -109,6 +111,12 @@ __device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_
       tmem_ld32(tbase + c * 32, v);
     }
     const int cvalid = valid - c * 32;   // > 0
+    if constexpr (kScaled) {
+      // e4m3 operands: z = acc * scale(row) * scale(column)
+      const float* wsc = wscale + n0 + c * 32;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= rscale * (j < cvalid ? __ldg(wsc + j) : 0.f);
+    }
     const int tj = tgt - (n0 + c * 32);
     if (static_cast<unsigned>(tj) < static_cast<unsigned>(cvalid < 32 ? cvalid : 32)) {
 #pragma unroll
@@ -385,6 +393,25 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// e4m3 k-block: 128 one-byte elements per 128-byte swizzle row.
+constexpr int kKbFp8 = 128;
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A/B (format code 0), an
+// fp32 accumulator, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                                uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -411,6 +438,9 @@ __device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {
                : "memory");
 }
 
+// kFp8 selects the e4m3 forward instantiation (jobs of kind kTcFwdFp8 only);
+// the bf16 instantiation carries none of its code.
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_constant__ TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -446,7 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R_pad;
       js[j].num_m = (M + kPM - 1) / kPM;
       js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
-      js[j].num_kb = (K + kTcBK - 1) / kTcBK;
+      constexpr int kbe = kFp8 ? kKbFp8 : kTcBK;
+      js[j].num_kb = (K + kbe - 1) / kbe;
       js[j].tiles = js[j].num_m * js[j].num_n;
       total += js[j].tiles;
     }
@@ -542,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
           uint8_t* dB = sB + stage * kPBBytes;
           const uint32_t bar = full_leader0 + 8 * stage;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPStageBytes);
-          const int k0 = kb * kTcBK;
-          if (kind == kTcFwd || kind == kTcDLogits) {
+          const int k0 = kb * (kFp8 ? kKbFp8 : kTcBK);
+          if (kFp8 || kind == kTcFwd || kind == kTcDLogits) {
             tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
             tma_load_2d_pair(dB, &jb.tmB, bar, k0, jb.v0 + ncol);
           } else if (kind == kTcDHidden) {
@@ -590,9 +621,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         if (t < 0) break;
         const Work w = locate(t, js, a.n_jobs, a);
         const int kind = a.jobs[w.job].kind;
-        const bool a_mn = (kind == kTcDWeight);
-        const bool b_mn = (kind == kTcDHidden || kind == kTcDWeight);
-        const uint32_t idesc = a_mn ? idesc_bf16_f32(kPM, kTcBN, true, true)
+        const bool a_mn = !kFp8 && (kind == kTcDWeight);
+        const bool b_mn = !kFp8 && (kind == kTcDHidden || kind == kTcDWeight);
+        const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPM, kTcBN)
+                                    : a_mn ? idesc_bf16_f32(kPM, kTcBN, true, true)
                                     : (b_mn ? idesc_bf16_f32(kPM, kTcBN, false, true)
                                             : idesc_bf16_f32(kPM, kTcBN, false, false));
         const uint32_t a_lbo = a_mn ? 8192 : 16, a_step = a_mn ? 2048 : 32;
@@ -616,11 +648,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
           tc_fence_after();
           const uint32_t a_addr = smem_u32(sA + stage * kPABytes);
           const uint32_t b_addr = smem_u32(sB + stage * kPBBytes);
+          // four MMAs per 128-byte k-block: K = 16 bf16 or 32 e4m3 each, so
+          // the K-major descriptors advance 32 bytes either way
 #pragma unroll
-          for (int k = 0; k < kTcBK / 16; ++k) {
+          for (int k = 0; k < 4; ++k) {
             const uint64_t adesc = sdesc_sw128(a_addr + k * a_step, a_lbo, 1024);
             const uint64_t bdesc = sdesc_sw128(b_addr + k * b_step, b_lbo, 1024);
-            umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            if constexpr (kFp8)
+              umma_e4m3_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            else
+              umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit_pair_both(&empty[stage]);
           if (++stage == kPStages) {
@@ -672,8 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       RowScalars rs;
       rs.active = false;
       bool active = false;
-      if (kind == kTcFwd) {
-        if (tok >= 0) tgt = a.targets[tok] - a.t_off;
+      float rscale = 0.f;
+      if (kFp8 || kind == kTcFwd) {
+        if (tok >= 0) {
+          tgt = a.targets[tok] - a.t_off;
+          if constexpr (kFp8) rscale = a.hscale[tok];
+        }
       } else if (kind == kTcDLogits) {
         active = (tok >= 0) && (a.mask[tok] != 0);
         rs.active = active;
@@ -695,10 +736,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
-      if (kind == kTcFwd) epi_fwd(a, tbase, k_empty, r0, w.tc.n, row, tgt);
-      else if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, r0, w.tc.n, row, rs);
-      else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
-      else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
+      if constexpr (kFp8) {
+        epi_fwd<true>(a, tbase, k_empty, r0, w.tc.n, row, tgt, rscale, a.wscale);
+      } else {
+        if (kind == kTcFwd) epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
+        else if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, r0, w.tc.n, row, rs);
+        else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
+        else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -727,12 +772,16 @@ int tc_tile_rows() { return kPM; }
 cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (args.n_jobs < 1 || args.n_jobs > kMaxTcJobs) return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(tc_pair_kernel,
+  // jobs of one launch are all e4m3 forward jobs or all bf16 jobs
+  const bool fp8 = (args.jobs[0].kind == kTcFwdFp8);
+  for (int j = 1; j < args.n_jobs; ++j)
+    if ((args.jobs[j].kind == kTcFwdFp8) != fp8) return cudaErrorInvalidValue;
+  static bool configured[2] = {false, false};
+  if (!configured[fp8]) {
+    cudaError_t e = cudaFuncSetAttribute(fp8 ? tc_pair_kernel<true> : tc_pair_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[fp8] = true;
   }
   const int clusters = (grid + 1) / 2;
   cudaLaunchConfig_t cfg;
@@ -748,7 +797,8 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tc_pair_kernel, args);
+  if (fp8) return cudaLaunchKernelEx(&cfg, tc_pair_kernel<true>, args);
+  return cudaLaunchKernelEx(&cfg, tc_pair_kernel<false>, args);
 }
 
 }  // namespace eas

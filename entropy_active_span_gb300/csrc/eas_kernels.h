@@ -52,6 +52,7 @@ enum TcKind : int {
   kTcDLogits = 1,  // Z = Hp W_c^T -> dZ_c (bf16 staging)
   kTcDHidden = 2,  // dHacc (+)= dZ_c W_c -> fp32 accumulator / final dhidden
   kTcDWeight = 3,  // dW_c = dZ_c^T Hp -> fp32 dW rows
+  kTcFwdFp8 = 4,   // as kTcFwd with e4m3 operands and per-row scales
 };
 
 // One contraction of a launch.  A launch runs up to kMaxTcJobs jobs; their
@@ -102,6 +103,8 @@ struct TcArgs {
   void* dhidden;          // bf16 [T][H]
   int H;
   float* dW;              // fp32 [V][H]
+  const float* hscale;    // e4m3 forward: per-token scale of hidden [T]
+  const float* wscale;    // e4m3 forward: per-row scale of W [V]
 };
 
 size_t tc_smem_bytes();
@@ -151,6 +154,9 @@ cudaError_t launch_simt_gemm(const SimtArgs& args, long long max_tiles, cudaStre
 }  // namespace eas
 
 namespace eas {
+// ---- e4m3 quantisation (eas_fp8.cu) ----
+cudaError_t launch_quantize_rows_e4m3(const void* src, int src_is_bf16, long long R, long long H,
+                                      uint8_t* dst, float* scale, int num_sms, cudaStream_t s);
 // ---- helpers the C-ABI translation units share (eas_api.cu) ----
 size_t lmhead_fwd_workspace_bytes(long long T, long long H, long long V, int dtype);
 void set_last_error(const char* msg);

@@ -68,7 +68,9 @@ typedef enum {
 
 typedef enum {
     EAS_BF16 = 0,   /* hidden, W, dhidden bf16; tensor cores, fp32 accumulate */
-    EAS_FP32 = 1    /* hidden, W, dhidden fp32; fp32 FMA throughout           */
+    EAS_FP32 = 1,   /* hidden, W, dhidden fp32; fp32 FMA throughout           */
+    EAS_E4M3 = 2    /* hidden, W in e4m3 with per-row fp32 scales; forward
+                       only (eas_lmhead_fwd_fp8), tensor cores             */
 } eas_dtype;
 
 /* Row policy for the forward/backward (the `flags` argument). */
@@ -189,6 +191,35 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy,
                           int64_t vocab_chunk,
                           void* dhidden, float* dweight,
                           void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------- e4m3 forward */
+
+/*
+ * Per-row e4m3 (FP8, 4 exponent bits, 3 mantissa bits, largest value 448)
+ * quantisation of a [R, H] bf16 or fp32 matrix: for each row
+ *   amax = max |x|, scale[r] = amax / 448, q = e4m3(x * (448 / amax))
+ * rounded to nearest-even and saturated at 448 (an all-zero row gets scale 1).
+ * The row's values are then approximately e4m3(q) * scale[r].
+ * dst [R, H] uint8 codes, scale [R] fp32 (device).
+ */
+eas_status eas_quantize_rows_e4m3(const void* src, eas_dtype src_dtype, int64_t R, int64_t H,
+                                  uint8_t* dst, float* scale, void* stream);
+
+/*
+ * Forward (logprob, entropy, lse) with e4m3 operands: the logit of token t
+ * and vocabulary row v is
+ *   z = hidden_scale[t] * weight_scale[v] * sum_h e4m3(hidden[t,h]) e4m3(W[v,h])
+ * accumulated in fp32 on the tensor cores (tcgen05 kind::f8f6f4); the rest is
+ * eas_lmhead_fwd.  For forward-only scoring; the backward takes bf16 or fp32.
+ * Requires H % 128 == 0.  Workspace: eas_lmhead_workspace_size(..., EAS_E4M3, 0).
+ */
+eas_status eas_lmhead_fwd_fp8(const uint8_t* hidden_e4m3, const float* hidden_scale,
+                              const uint8_t* weight_e4m3, const float* weight_scale,
+                              const int32_t* targets, const uint8_t* mask,
+                              const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                              int64_t T, int64_t H, int64_t V, uint32_t flags,
+                              float* logprob, float* entropy, float* lse,
+                              void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------ vocabulary-parallel path */
 
