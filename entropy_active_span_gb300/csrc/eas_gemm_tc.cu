@@ -438,10 +438,14 @@ __device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {
                : "memory");
 }
 
-// kFp8 selects the e4m3 forward instantiation (jobs of kind kTcFwdFp8 only);
-// the bf16 instantiation carries none of its code.
-template <bool kFp8>
+// One instantiation per family of jobs, so that each carries only the code
+// its jobs run (the kernel's size measurably costs throughput):
+//   kMode 0: bf16 forward (kTcFwd), 1: bf16 backward (kTcDLogits, kTcDHidden,
+//   kTcDWeight), 2: e4m3 forward (kTcFwdFp8).
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_constant__ TcArgs a) {
+  constexpr bool kFp8 = (kMode == 2);
+  constexpr bool kFwd = (kMode != 1);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
           const uint32_t bar = full_leader0 + 8 * stage;
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPStageBytes);
           const int k0 = kb * (kFp8 ? kKbFp8 : kTcBK);
-          if (kFp8 || kind == kTcFwd || kind == kTcDLogits) {
+          if (kFwd || kind == kTcDLogits) {
             tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
             tma_load_2d_pair(dB, &jb.tmB, bar, k0, jb.v0 + ncol);
           } else if (kind == kTcDHidden) {
@@ -621,8 +625,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         if (t < 0) break;
         const Work w = locate(t, js, a.n_jobs, a);
         const int kind = a.jobs[w.job].kind;
-        const bool a_mn = !kFp8 && (kind == kTcDWeight);
-        const bool b_mn = !kFp8 && (kind == kTcDHidden || kind == kTcDWeight);
+        const bool a_mn = !kFwd && (kind == kTcDWeight);
+        const bool b_mn = !kFwd && (kind == kTcDHidden || kind == kTcDWeight);
         const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPM, kTcBN)
                                     : a_mn ? idesc_bf16_f32(kPM, kTcBN, true, true)
                                     : (b_mn ? idesc_bf16_f32(kPM, kTcBN, false, true)
@@ -710,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       rs.active = false;
       bool active = false;
       float rscale = 0.f;
-      if (kFp8 || kind == kTcFwd) {
+      if (kFwd) {
         if (tok >= 0) {
           tgt = a.targets[tok] - a.t_off;
           if constexpr (kFp8) rscale = a.hscale[tok];
@@ -738,9 +742,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
       if constexpr (kFp8) {
         epi_fwd<true>(a, tbase, k_empty, r0, w.tc.n, row, tgt, rscale, a.wscale);
+      } else if constexpr (kFwd) {
+        epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
       } else {
-        if (kind == kTcFwd) epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
-        else if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, r0, w.tc.n, row, rs);
+        if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, r0, w.tc.n, row, rs);
         else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
         else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
       }
@@ -772,16 +777,19 @@ int tc_tile_rows() { return kPM; }
 cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (args.n_jobs < 1 || args.n_jobs > kMaxTcJobs) return cudaErrorInvalidValue;
-  // jobs of one launch are all e4m3 forward jobs or all bf16 jobs
-  const bool fp8 = (args.jobs[0].kind == kTcFwdFp8);
+  // the jobs of one launch belong to one family (see tc_pair_kernel)
+  auto family = [](int kind) { return kind == kTcFwd ? 0 : kind == kTcFwdFp8 ? 2 : 1; };
+  const int mode = family(args.jobs[0].kind);
   for (int j = 1; j < args.n_jobs; ++j)
-    if ((args.jobs[j].kind == kTcFwdFp8) != fp8) return cudaErrorInvalidValue;
-  static bool configured[2] = {false, false};
-  if (!configured[fp8]) {
-    cudaError_t e = cudaFuncSetAttribute(fp8 ? tc_pair_kernel<true> : tc_pair_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+    if (family(args.jobs[j].kind) != mode) return cudaErrorInvalidValue;
+  static bool configured[3] = {false, false, false};
+  void (*kern)(TcArgs) = mode == 0 ? tc_pair_kernel<0> : mode == 1 ? tc_pair_kernel<1>
+                                                                    : tc_pair_kernel<2>;
+  if (!configured[mode]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kPSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[fp8] = true;
+    configured[mode] = true;
   }
   const int clusters = (grid + 1) / 2;
   cudaLaunchConfig_t cfg;
@@ -797,8 +805,7 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (fp8) return cudaLaunchKernelEx(&cfg, tc_pair_kernel<true>, args);
-  return cudaLaunchKernelEx(&cfg, tc_pair_kernel<false>, args);
+  return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
 }  // namespace eas
