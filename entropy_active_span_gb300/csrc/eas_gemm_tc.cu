@@ -218,9 +218,19 @@ __device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, ui
           const float x2 = fmaf(v[j], kLog2e, -rs.lse2);    // (z - lse) log2 e
           const float p = ex2_approx(x2);
           const float w = fmaf(rs.gh2, x2, rs.c1);           // g_H (z - lse) + g_lp + g_H H
-          float dz = -p * w;
-          if (j == tj) dz += rs.glp;
-          d[j] = (j < cvalid) ? dz : 0.f;
+          d[j] = -p * w;
+        }
+        // the target column and the live-width edge fall in few chunks:
+        // branch around them instead of selecting on every element
+        if (static_cast<unsigned>(tj) < 32u) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == tj) d[j] += rs.glp;
+        }
+        if (cvalid < 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j >= cvalid) d[j] = 0.f;
         }
 #pragma unroll
         for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(d[2 * j], d[2 * j + 1]);
