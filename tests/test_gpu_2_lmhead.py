@@ -243,3 +243,40 @@ def test_very_large_logits_stay_finite_and_match():
     for k in got:
         assert np.all(np.isfinite(got[k])), k
     check(got, oracle_all(inp), inp["mask"], BF16_TOL)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_single_word_vocabulary(dtype):
+    """V = 1: every softmax is the point mass, so logprob = entropy = 0 and
+    all gradients vanish; lse is the single logit."""
+    inp = small_inputs(300, 128, 1, dtype=dtype, seed=2, mask_kind="bernoulli0.7", w_std=3.0)
+    got = run_gpu(inp)
+    ref = oracle_all(inp)
+    assert np.max(np.abs(got["logprob"])) <= 1e-6 and np.max(np.abs(got["entropy"])) <= 1e-6
+    assert np.max(np.abs(got["lse"] - ref["lse"])) <= BF16_TOL["lp"]
+    # p = 2^((z - lse) log2 e) is 1 only up to ex2 rounding (~1e-7), so the
+    # d-logits are ~1e-7 g_lp and the gradients ~1e-7 |W|, not exact zeros
+    assert np.max(np.abs(got["dhidden"])) <= 1e-4 and np.max(np.abs(got["dweight"])) <= 1e-4
+
+
+def test_two_word_vocabulary():
+    inp = small_inputs(500, 128, 2, seed=4, mask_kind="bernoulli0.7", w_std=6.0)
+    got = run_gpu(inp)
+    check(got, oracle_all(inp), inp["mask"], BF16_TOL)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_zero_tokens(dtype):
+    H, V = 128, 300
+    h = torch.empty((0, H), dtype=dtype, device="cuda")
+    w = torch.randn((V, H), device="cuda").to(dtype)
+    t = torch.empty(0, dtype=torch.int32, device="cuda")
+    m = torch.empty(0, dtype=torch.uint8, device="cuda")
+    spans, ns = eas.build_active_spans(m, 128)
+    assert int(ns.item()) == 0
+    lp, ent, lse = eas.lmhead_fwd(h, w, t, m, spans, ns)
+    assert lp.numel() == 0
+    g = torch.empty(0, device="cuda")
+    dh, dw = eas.lmhead_bwd(g, g, h, w, t, m, spans, ns, lse, ent)
+    torch.cuda.synchronize()
+    assert dh.shape == (0, H) and torch.all(dw == 0)
