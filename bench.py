@@ -311,8 +311,11 @@ def main():
     def step(m=mask):
         eas.build_active_spans(m, args.max_gap, spans=spans, num_spans=ns, ws=sws)
         eas.lmhead_fwd(hidden, weight, targets, m, spans, ns, flags, ws=ws, out=(lp, ent, lse))
-        eas.lmhead_bwd(glp, gh, hidden, weight, targets, m, spans, ns, lse, ent, flags,
-                       args.vocab_chunk, ws=ws, dhidden=dh, dweight=dw)
+        # the backward reuses the row schedule and packed rows the forward
+        # just left in the same workspace
+        eas.lmhead_bwd(glp, gh, hidden, weight, targets, m, spans, ns, lse, ent,
+                       flags | eas.EAS_REUSE_FWD_ROWS, args.vocab_chunk, ws=ws, dhidden=dh,
+                       dweight=dw)
 
     def barrier():
         if world > 1:
@@ -466,7 +469,8 @@ def main():
                                spans, ns, flags, ws=ws, out=(lp, ent, lse))
                 eas.lmhead_bwd(d_in["g_logprob"], d_in["g_entropy"], d_in["hidden"],
                                d_in["weight"], d_in["targets"], d_in["mask"], spans, ns, lse, ent,
-                               flags, args.vocab_chunk, ws=ws, dhidden=dh, dweight=dw)
+                               flags | eas.EAS_REUSE_FWD_ROWS, args.vocab_chunk, ws=ws,
+                               dhidden=dh, dweight=dw)
                 free[b].record(stream)
                 out_lp.copy_(lp, non_blocking=True)
                 out_ent.copy_(ent, non_blocking=True)

@@ -15,13 +15,14 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (EAS_BF16, EAS_DEFAULT_VOCAB_CHUNK, EAS_E4M3, EAS_FP32, EAS_ROWS_ACTIVE,
-                   EAS_ROWS_SPAN, EasError)
+from ._lib import (EAS_BF16, EAS_DEFAULT_VOCAB_CHUNK, EAS_E4M3, EAS_FP32, EAS_REUSE_FWD_ROWS,
+                   EAS_ROWS_ACTIVE, EAS_ROWS_SPAN, EasError)
 
 __all__ = [
     "build_active_spans", "lmhead_fwd", "lmhead_bwd", "lmhead_workspace_size",
     "spans_workspace_size", "read_device_status", "workspace", "EasError",
-    "EAS_ROWS_ACTIVE", "EAS_ROWS_SPAN", "EAS_DEFAULT_VOCAB_CHUNK", "FusedLMHeadLogprob",
+    "EAS_ROWS_ACTIVE", "EAS_ROWS_SPAN", "EAS_REUSE_FWD_ROWS", "EAS_DEFAULT_VOCAB_CHUNK",
+    "FusedLMHeadLogprob",
     "fused_logprob_entropy", "trace_enable", "trace_read", "lmhead_fwd_shard",
     "lmhead_combine_shards", "lmhead_bwd_shard", "cp_local_layout", "quantize_rows_e4m3",
     "lmhead_fwd_fp8",

@@ -23,6 +23,7 @@ EAS_E4M3 = 2
 
 EAS_ROWS_ACTIVE = 0
 EAS_ROWS_SPAN = 1
+EAS_REUSE_FWD_ROWS = 2
 
 EAS_DEFAULT_VOCAB_CHUNK = 16384
 EAS_STATIC_SCRATCH_BYTES = 64 << 20

@@ -205,10 +205,10 @@ struct Layout {
   long long vc;        // vocabulary chunk of the backward
   int n_chunks;
   long long ldz;       // staging row pitch (elements)
-  size_t status, sched, counters, head_end;      // cleared at the start of each call
+  size_t status, sched, head_end;                // cleared at the start of each call
   size_t row_map, pack_of, hp;                   // common part
-  size_t pm, ps, pu, zt;                          // forward part
-  size_t dz, dz2, acc;                            // backward part (two staging buffers)
+  size_t pm, ps, pu, zt, fwd_counter;             // forward part
+  size_t dz, dz2, acc, counters;                  // backward part (two staging buffers)
   size_t fwd_end, bwd_end, total;
 };
 
@@ -227,7 +227,6 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   size_t o = 0;
   L.status = o; o = align_up(o + sizeof(DevStatus));
   L.sched = o; o = align_up(o + sizeof(Sched));
-  L.counters = o; o = align_up(o + sizeof(int) * static_cast<size_t>(L.n_chunks + 2));
   L.head_end = o;
   L.row_map = o; o = align_up(o + 4 * static_cast<size_t>(L.T_pad > 0 ? L.T_pad : 1));
   L.pack_of = o; o = align_up(o + 4 * static_cast<size_t>(T > 0 ? T : 1));
@@ -237,6 +236,7 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   L.ps = o; o = align_up(o + 4 * static_cast<size_t>(L.n_vt) * L.T_pad);
   L.pu = o; o = align_up(o + 4 * static_cast<size_t>(L.n_vt) * L.T_pad);
   L.zt = o; o = align_up(o + 4 * static_cast<size_t>(L.T_pad));
+  L.fwd_counter = o; o = align_up(o + sizeof(int));
   L.fwd_end = o;
   o = common;
   L.dz = o; o = align_up(o + esz * static_cast<size_t>(L.T_pad) * L.ldz);
@@ -244,6 +244,7 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   if (dt == EAS_BF16 && L.n_chunks > 1) o = align_up(o + esz * static_cast<size_t>(L.T_pad) * L.ldz);
   L.acc = o;
   if (L.n_chunks > 1) o = align_up(o + 4 * static_cast<size_t>(L.T_pad) * H);
+  L.counters = o; o = align_up(o + sizeof(int) * static_cast<size_t>(L.n_chunks + 1));
   L.bwd_end = o;
   L.total = L.fwd_end > L.bwd_end ? L.fwd_end : L.bwd_end;
   return L;
@@ -412,7 +413,7 @@ static eas_status fwd_impl(const void* hidden, const void* weight, const int32_t
     a.n_jobs = 1;
     a.sched = sched;
     a.status = at<DevStatus>(ws, L.status);
-    a.tile_counter = at<int>(ws, L.counters);
+    a.tile_counter = at<int>(ws, L.fwd_counter);
     a.budget = wait_budget();
     a.row_map = at<int>(ws, L.row_map);
     a.targets = targets;
@@ -424,6 +425,10 @@ static eas_status fwd_impl(const void* hidden, const void* weight, const int32_t
     a.part_stride = L.T_pad;
     a.V = static_cast<int>(V);
     a.H = static_cast<int>(H);
+    {
+      Trace tr_(kTrMemset, s);
+      EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.fwd_counter), 0, sizeof(int), s), "clear counter");
+    }
     {
       Trace tr_(kTrFwdGemm, s);
       EAS_CUDA(launch_tc_gemm(a, grid_for(num_m_max * L.n_vt, di.sms), s), "fwd gemm");
@@ -553,6 +558,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
   if (st != EAS_OK) return st;
   if (dtype == EAS_E4M3)
     return fail(EAS_ERR_UNSUPPORTED, "the backward takes bf16 or fp32 operands");
+  const bool reuse = (flags & EAS_REUSE_FWD_ROWS) != 0;
+  flags &= ~EAS_REUSE_FWD_ROWS;
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
   if (cap < 0) return fail(EAS_ERR_INVALID_ARG, "cap must be >= 0");
   if (vocab_chunk < 0) return fail(EAS_ERR_INVALID_ARG, "vocab_chunk must be >= 0");
@@ -570,9 +577,19 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
   if (st != EAS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-  st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, targets, 0,
-                sharded ? 0x7fffffffLL : static_cast<long long>(V), ws, L, di, s);
-  if (st != EAS_OK) return st;
+  if (!reuse) {
+    st = prologue(hidden, mask, spans, num_spans, cap, T, H, dtype, flags, targets, 0,
+                  sharded ? 0x7fffffffLL : static_cast<long long>(V), ws, L, di, s);
+    if (st != EAS_OK) return st;
+  }
+  // (with reuse, the row schedule and packed rows of the preceding forward
+  // stay where that call's layout put them: the shared part of the layout
+  // does not depend on vocab_chunk; the status word is kept)
+  {
+    Trace tr_(kTrMemset, s);
+    EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.counters), 0, sizeof(int) * (L.n_chunks + 1), s),
+             "clear counters");
+  }
   if (T == 0) {
     {
       Trace tr_(kTrMemset, s);

@@ -80,6 +80,14 @@ typedef enum {
                                (span-contiguous schedule; gap rows still get
                                zero outputs and gradients)                  */
 
+/* Backward only: the workspace still holds what eas_lmhead_fwd left in it
+ * for the same hidden, mask, spans and row policy, enqueued before on the same
+ * stream with nothing else touching the workspace in between.  The backward
+ * then reuses that call's row schedule and packed hidden rows instead of
+ * rebuilding them, and keeps its status word instead of clearing it.  The
+ * backward's vocab_chunk does not matter for this. */
+#define EAS_REUSE_FWD_ROWS 2u
+
 /* Default vocabulary chunk width of the backward (columns of d-logits held
  * in the staging buffer at once).  0 passed as vocab_chunk selects it. */
 #define EAS_DEFAULT_VOCAB_CHUNK 16384

@@ -280,3 +280,25 @@ def test_zero_tokens(dtype):
     dh, dw = eas.lmhead_bwd(g, g, h, w, t, m, spans, ns, lse, ent)
     torch.cuda.synchronize()
     assert dh.shape == (0, H) and torch.all(dw == 0)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+@pytest.mark.parametrize("rows", [eas.EAS_ROWS_ACTIVE, eas.EAS_ROWS_SPAN])
+def test_backward_reusing_forward_rows_is_bitwise_equal(dtype, rows):
+    inp = small_inputs(1100, 256, 1300, dtype=dtype, seed=8, mask_kind="bernoulli0.5", w_std=3.0)
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
+    spans, ns = eas.build_active_spans(m, 128)
+    T, H = h.shape
+    V = w.shape[0]
+    ws = eas.workspace(eas.lmhead_workspace_size(T, H, V, h.dtype, 384), "cuda")
+    lp, ent, lse = eas.lmhead_fwd(h, w, t, m, spans, ns, rows, ws=ws)
+    ref = eas.lmhead_bwd(glp, gh, h, w, t, m, spans, ns, lse, ent, rows, 384, ws=ws)
+    ref = [x.clone() for x in ref]
+    eas.lmhead_fwd(h, w, t, m, spans, ns, rows, ws=ws, out=(lp, ent, lse))
+    got = eas.lmhead_bwd(glp, gh, h, w, t, m, spans, ns, lse, ent,
+                         rows | eas.EAS_REUSE_FWD_ROWS, 384, ws=ws)
+    assert eas.read_device_status(ws) == 0
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
