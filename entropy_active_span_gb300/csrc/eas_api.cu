@@ -10,8 +10,8 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <deque>
 #include <mutex>
-#include <vector>
 
 #include "../../include/eas.h"
 #include "eas_device.cuh"
@@ -114,7 +114,8 @@ struct TraceRec {
 
 std::mutex g_trace_mu;
 bool g_trace_on = false;
-std::vector<TraceRec> g_trace_pool;   // events are created once and reused
+std::deque<TraceRec> g_trace_pool;    // events are created once and reused; a deque
+                                      // keeps records in place as it grows
 size_t g_trace_used = 0;
 
 class Trace {

@@ -302,3 +302,23 @@ def test_backward_reusing_forward_rows_is_bitwise_equal(dtype, rows):
     assert eas.read_device_status(ws) == 0
     for a, b in zip(ref, got):
         assert torch.equal(a, b)
+
+
+def test_trace_records_every_launch():
+    inp = small_inputs(600, 256, 1200, seed=12, mask_kind="bernoulli0.6")
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
+    eas.trace_enable(True)
+    spans, ns = eas.build_active_spans(m, 128)
+    lp, ent, lse = eas.lmhead_fwd(h, w, t, m, spans, ns)
+    eas.lmhead_bwd(glp, gh, h, w, t, m, spans, ns, lse, ent, vocab_chunk=512)
+    eas.trace_enable(False)
+    recs = eas.trace_read()
+    names = [n for n, _ in recs]
+    for k in ("spans_build", "rowmap", "gather_rows", "fwd_gemm_tc", "combine",
+              "dlogits_gemm_tc", "bwd_chunk_gemm_tc", "dproj_gemm_tc", "zero_rows"):
+        assert k in names, k
+    # three vocabulary chunks: d-logits(0), two chunk launches, the last projections
+    assert names.count("bwd_chunk_gemm_tc") == 2 and names.count("dproj_gemm_tc") == 1
+    assert all(ms >= 0 for _, ms in recs)
