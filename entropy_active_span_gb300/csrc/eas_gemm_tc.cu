@@ -487,7 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
     if (j < a.n_jobs) {
       const TcJob& jb = a.jobs[j];
       const int M = jb.M_fixed > 0 ? jb.M_fixed : sched->R_pad;
-      const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R_pad;
+      // a reduction over packed rows (dW) stops at the last k-block holding a
+      // real row; rows from R to R_pad are zero in both operands
+      const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R;
       js[j].num_m = (M + kPM - 1) / kPM;
       js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
       constexpr int kbe = kFp8 ? kKbFp8 : kTcBK;

@@ -65,7 +65,7 @@ struct TcJob {
   int kind;
   int M_fixed;       // > 0: rows of the problem; 0: R_pad from sched
   int N;             // columns of the problem
-  int K_fixed;       // > 0: reduction length; 0: R_pad from sched
+  int K_fixed;       // > 0: reduction length; 0: the packed row count R from sched
   int group_m;       // m-tiles per raster band
   int v0;            // first vocabulary row of the chunk (B row / k offset)
   int vc_live;       // live columns of this chunk (dlogits / dweight)
