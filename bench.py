@@ -76,7 +76,9 @@ def parse_args():
     p.add_argument("--no-forward-only", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
-                   help="target CPU time of the oracle sample")
+                   help="target CPU time of the oracle sample (cpu_baseline)")
+    p.add_argument("--ref-step-seconds", type=float, default=2.0,
+                   help="target CPU time of one --impl reference step")
     return p.parse_args()
 
 
@@ -132,27 +134,43 @@ def host_cores() -> int:
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample_rate(inp, target_s: float):
-    """Times the fp64 oracle's fwd+bwd on a sample of active rows (rows/s)."""
+def _oracle_rows(inp, rows, Wf):
+    """One oracle fwd+bwd over the given active rows; returns seconds."""
     import oracle
+    h = W.to_f64(inp["hidden"][rows])
+    t0 = time.perf_counter()
+    oracle.lmhead_forward_rows(h, Wf, inp["targets"][rows])
+    oracle.lmhead_backward_rows_weighted(h, Wf, inp["targets"][rows],
+                                         inp["g_logprob"][rows], inp["g_entropy"][rows])
+    return time.perf_counter() - t0
+
+
+def oracle_sample_size(inp, Wf, target_s: float, rng) -> int:
+    """Active rows whose oracle fwd+bwd takes about target_s on this host.
+
+    The oracle's cost per row falls as batches grow (small batches are
+    memory-bound on W), so the estimate comes from a batch that already takes
+    a good fraction of a second, doubling from 8 rows."""
+    act = np.flatnonzero(inp["mask"])
+    n = 8
+    while True:
+        rows = np.sort(rng.choice(act, size=min(n, len(act)), replace=False))
+        t = _oracle_rows(inp, rows, Wf)
+        if t >= 0.25 * target_s or len(rows) == len(act) or n >= 1 << 20:
+            break
+        n *= 2
+    return int(max(8, min(len(act), len(rows) * target_s / max(t, 1e-9))))
+
+
+def oracle_sample_rate(inp, target_s: float):
+    """Times the fp64 oracle's fwd+bwd on a sample of active rows sized to
+    about target_s seconds.  Returns (rows, seconds)."""
     act = np.flatnonzero(inp["mask"])
     Wf = W.to_f64(inp["weight"])
     rng = np.random.default_rng(0)
-
-    def run(n):
-        rows = np.sort(rng.choice(act, size=min(n, len(act)), replace=False))
-        h = W.to_f64(inp["hidden"][rows])
-        t0 = time.perf_counter()
-        oracle.lmhead_forward_rows(h, Wf, inp["targets"][rows])
-        oracle.lmhead_backward_rows_weighted(h, Wf, inp["targets"][rows],
-                                             inp["g_logprob"][rows], inp["g_entropy"][rows])
-        return len(rows), time.perf_counter() - t0
-
-    n0, t0 = run(8)
-    per_row = t0 / max(n0, 1)
-    n = int(max(8, min(len(act), target_s / max(per_row, 1e-9))))
-    n, t = run(n)
-    return n, t
+    n = oracle_sample_size(inp, Wf, target_s, rng)
+    rows = np.sort(rng.choice(act, size=n, replace=False))
+    return n, _oracle_rows(inp, rows, Wf)
 
 
 def reference_arm(args, rank):
@@ -161,28 +179,17 @@ def reference_arm(args, rank):
         return
     w = W.ALL_WORKLOADS[args.workload]
     inp = W.make_inputs(w)
-    import oracle
     act = np.flatnonzero(inp["mask"])
     Wf = W.to_f64(inp["weight"])
     rng = np.random.default_rng(1)
-    # size the per-step sample so one step is about args.cpu_seconds / 2
-    h8 = W.to_f64(inp["hidden"][act[:8]])
-    t0 = time.perf_counter()
-    oracle.lmhead_forward_rows(h8, Wf, inp["targets"][act[:8]])
-    oracle.lmhead_backward_rows_weighted(h8, Wf, inp["targets"][act[:8]],
-                                         inp["g_logprob"][act[:8]], inp["g_entropy"][act[:8]])
-    per_row = (time.perf_counter() - t0) / 8
-    n = int(max(8, min(len(act), 0.5 * args.cpu_seconds / max(per_row, 1e-9))))
+    # one step = a sample of active rows sized to about --ref-step-seconds
+    n = oracle_sample_size(inp, Wf, args.ref_step_seconds, rng)
     times = []
     for i in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(act, size=n, replace=False))
-        h = W.to_f64(inp["hidden"][rows])
-        t0 = time.perf_counter()
-        oracle.lmhead_forward_rows(h, Wf, inp["targets"][rows])
-        oracle.lmhead_backward_rows_weighted(h, Wf, inp["targets"][rows],
-                                             inp["g_logprob"][rows], inp["g_entropy"][rows])
+        t = _oracle_rows(inp, rows, Wf)
         if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
+            times.append(t)
     total = sum(times)
     value = n * len(times) / total
     cores = host_cores()
