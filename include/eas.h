@@ -41,6 +41,9 @@
  *     of time) are written to a status word inside the workspace; read it with
  *     eas_read_device_status().  The status word is cleared at the start of
  *     every call that takes the workspace.
+ *   - A workspace belongs to one call at a time: two calls whose kernels may
+ *     run at the same time on the GPU (different streams, or threads without
+ *     ordering) need different workspaces.
  *   - eas_last_error() returns a thread-local message about the last error.
  */
 #ifndef EAS_H_
