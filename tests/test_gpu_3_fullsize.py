@@ -1,6 +1,8 @@
 """GPU parity at the five workloads' full sizes, in the launch configuration
 bench.py times (spans with max_gap 128, active-row schedule, default vocab
-chunk).
+chunk); packed_64k runs once more with the span-contiguous row schedule (the
+workload where the two schedules differ most) and rl_16k once more with a
+large-std W, so that the softmax is peaked rather than near-uniform.
 
 The oracle cannot afford whole problems here, so:
   * logprob / entropy / lse and dHidden are row-local: sampled rows (first and
@@ -40,10 +42,18 @@ def sample_rows(mask, spans, rng, n_random=48):
     return np.array(sorted(picks), np.int64)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "rl_16k", "packed_64k", "sparse_128k", "long_256k"])
-def test_full_size_workload(name):
+# W std 1.5 at H=4096 gives logits of std ~1.9: a peaked softmax (entropy well
+# below log V, target probabilities far from 1/V) at the full shape
+@pytest.mark.parametrize("name,row_policy,w_std", [("tiny_fp32", eas.EAS_ROWS_ACTIVE, None),
+                                                   ("rl_16k", eas.EAS_ROWS_ACTIVE, None),
+                                                   ("rl_16k", eas.EAS_ROWS_ACTIVE, 1.5),
+                                                   ("packed_64k", eas.EAS_ROWS_ACTIVE, None),
+                                                   ("packed_64k", eas.EAS_ROWS_SPAN, None),
+                                                   ("sparse_128k", eas.EAS_ROWS_ACTIVE, None),
+                                                   ("long_256k", eas.EAS_ROWS_ACTIVE, None)])
+def test_full_size_workload(name, row_policy, w_std):
     w = W.WORKLOADS[name]
-    inp = W.make_inputs(w)
+    inp = W.make_inputs(w, w_std=w_std)
     tol = FP32_TOL if w.dtype == "fp32" else BF16_TOL
     T, H, V = w.T, w.H, w.V
     mask_np = inp["mask"]
@@ -52,9 +62,10 @@ def test_full_size_workload(name):
     glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
     spans, ns = eas.build_active_spans(mask, 128)
     ws = eas.workspace(eas.lmhead_workspace_size(T, H, V, hidden.dtype), hidden.device)
-    lp, ent, lse = eas.lmhead_fwd(hidden, weight, targets, mask, spans, ns, ws=ws)
+    lp, ent, lse = eas.lmhead_fwd(hidden, weight, targets, mask, spans, ns, row_policy, ws=ws)
     assert eas.read_device_status(ws) == 0
-    dh, dw = eas.lmhead_bwd(glp, gh, hidden, weight, targets, mask, spans, ns, lse, ent, ws=ws)
+    dh, dw = eas.lmhead_bwd(glp, gh, hidden, weight, targets, mask, spans, ns, lse, ent,
+                            row_policy, ws=ws)
     assert eas.read_device_status(ws) == 0
     n = int(ns.item())
     spans_np = spans[:n].cpu().numpy().astype(np.int64)
@@ -70,6 +81,8 @@ def test_full_size_workload(name):
     W64 = W.to_f64(inp["weight"])
     h_rows = W.to_f64(inp["hidden"][rows])
     rlp, rent, rlse = oracle.lmhead_forward_rows(h_rows, W64, inp["targets"][rows])
+    if w_std is not None:   # the case is only worth its cost if the softmax is far from uniform
+        assert np.median(rent) < np.log(V) - 1.0
     ridx = torch.from_numpy(rows).cuda()
     assert np.max(np.abs(lp[ridx].cpu().numpy() - rlp)) <= tol["lp"]
     assert np.max(np.abs(ent[ridx].cpu().numpy() - rent)) <= tol["ent"]
@@ -86,7 +99,7 @@ def test_full_size_workload(name):
     g1[S] = inp["g_logprob"][S]
     g2[S] = inp["g_entropy"][S]
     dh2, dw2 = eas.lmhead_bwd(to_dev(g1), to_dev(g2), hidden, weight, targets, mask, spans, ns,
-                              lse, ent, ws=ws)
+                              lse, ent, row_policy, ws=ws)
     assert eas.read_device_status(ws) == 0
     rdh, rdw = oracle.lmhead_backward_rows_weighted(W.to_f64(inp["hidden"][S]), W64,
                                                     inp["targets"][S], g1[S], g2[S])
