@@ -180,65 +180,104 @@ struct RowScalars {
   bool active;
 };
 
-// d-logits of one row: dZ = g_lp (onehot - p) - g_H p (z - lse + H), p =
-// exp(z - lse), written as -p (g_H (z - lse) + g_lp + g_H H) + g_lp onehot.
-// Inactive rows and columns past the live width are written as exact zeros.
+// Coalesced row stores.  tcgen05.ld (32x32b) hands each lane one row of the
+// tile, so a lane storing its own row would touch 32 rows (32 memory lines)
+// per warp store.  octet_transpose regroups a chunk across each group of 8
+// lanes: on entry lane i of an octet holds 16-byte blocks b = 0..7 of its own
+// row (x[4b .. 4b+3]); on exit it holds block i of the octet's rows p = 0..7
+// (x[4p .. 4p+3]), so every store instruction writes 4 rows x 128 contiguous
+// bytes.  Three butterfly stages (lane xor 1, 2, 4) each swap half the blocks.
+template <typename T>
+__device__ __forceinline__ void octet_transpose(T (&x)[32], int i) {
+#pragma unroll
+  for (int s = 1; s < 8; s <<= 1) {
+    const bool hi = (i & s) != 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      if (b & s) continue;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const T send = hi ? x[4 * b + w] : x[4 * (b | s) + w];
+        const T recv = __shfl_xor_sync(0xffffffffu, send, s);
+        if (hi) x[4 * b + w] = recv;
+        else x[4 * (b | s) + w] = recv;
+      }
+    }
+  }
+}
+
+// d-logits of 32 columns of one row, packed to bf16 pairs: dZ = g_lp (onehot
+// - p) - g_H p (z - lse + H), p = exp(z - lse), written as -p (g_H (z - lse)
+// + g_lp + g_H H) + g_lp onehot.  Inactive rows and columns past the live
+// width are exact zeros.
+__device__ __forceinline__ void dlogits_chunk(const TcJob& jb, uint32_t taddr, bool k_empty,
+                                              int col0, const RowScalars& rs, uint32_t* pk) {
+  // tcgen05.ld is warp-collective: only warp-uniform conditions (live width,
+  // empty K) may skip it; per-row activity is applied afterwards.
+  if (col0 >= jb.vc_live) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+    return;
+  }
+  float v[32];
+  if (k_empty) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+  } else {
+    tmem_ld32(taddr, v);
+  }
+  if (!rs.active) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pk[j] = 0u;
+    return;
+  }
+  const int cvalid = jb.vc_live - col0;
+  const int tj = rs.tgt - col0;
+  float d[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float x2 = fmaf(v[j], kLog2e, -rs.lse2);    // (z - lse) log2 e
+    const float p = ex2_approx(x2);
+    const float w = fmaf(rs.gh2, x2, rs.c1);           // g_H (z - lse) + g_lp + g_H H
+    d[j] = -p * w;
+  }
+  // the target column and the live-width edge fall in few chunks: branch
+  // around them instead of selecting on every element
+  if (static_cast<unsigned>(tj) < 32u) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j == tj) d[j] += rs.glp;
+  }
+  if (cvalid < 32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j >= cvalid) d[j] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(d[2 * j], d[2 * j + 1]);
+}
+
+// d-logits tile rows into the bf16 staging buffer, 64 columns (128 bytes of a
+// row) per round.
 __device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, uint32_t tbase,
                                             bool k_empty, long long r0, int n_blk, int row,
                                             const RowScalars& rs) {
-  const long long r = r0 + row;
   const int n0 = n_blk * kTcBN;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(jb.dz) + r * a.ldz + n0;
+  const int lane = row & 31;
+  const int i = lane & 7;
+  const long long r_oct = r0 + (row & ~31) + (lane & ~7);   // first row of this octet
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(jb.dz) + r_oct * a.ldz + n0;
 #pragma unroll 1
-  for (int c = 0; c < kTcBN / 32; ++c) {
-    uint32_t pk[16];
-    const int col0 = n0 + c * 32;
-    // tcgen05.ld is warp-collective: only warp-uniform conditions (live
-    // width, empty K) may skip it; per-row activity is applied afterwards.
-    if (col0 >= jb.vc_live) {
+  for (int c = 0; c < kTcBN / 64; ++c) {
+    uint32_t pk[32];
+    dlogits_chunk(jb, tbase + c * 64, k_empty, n0 + c * 64, rs, pk);
+    dlogits_chunk(jb, tbase + c * 64 + 32, k_empty, n0 + c * 64 + 32, rs, pk + 16);
+    octet_transpose(pk, i);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) pk[j] = 0u;
-    } else {
-      float v[32];
-      if (k_empty) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-      } else {
-        tmem_ld32(tbase + c * 32, v);
-      }
-      if (!rs.active) {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = 0u;
-      } else {
-        const int cvalid = jb.vc_live - col0;
-        const int tj = rs.tgt - col0;
-        float d[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x2 = fmaf(v[j], kLog2e, -rs.lse2);    // (z - lse) log2 e
-          const float p = ex2_approx(x2);
-          const float w = fmaf(rs.gh2, x2, rs.c1);           // g_H (z - lse) + g_lp + g_H H
-          d[j] = -p * w;
-        }
-        // the target column and the live-width edge fall in few chunks:
-        // branch around them instead of selecting on every element
-        if (static_cast<unsigned>(tj) < 32u) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j == tj) d[j] += rs.glp;
-        }
-        if (cvalid < 32) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j >= cvalid) d[j] = 0.f;
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(d[2 * j], d[2 * j + 1]);
-      }
+    for (int p = 0; p < 8; ++p) {
+      uint4* o = reinterpret_cast<uint4*>(out + p * a.ldz + c * 64) + i;
+      *o = make_uint4(pk[4 * p], pk[4 * p + 1], pk[4 * p + 2], pk[4 * p + 3]);
     }
-    uint4* o = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
   }
 }
 
@@ -248,12 +287,22 @@ __device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, ui
 __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, uint32_t tbase,
                                             bool k_empty, long long r0, int n_blk, int row, int tok,
                                             bool active) {
-  const long long r = r0 + row;
   const int n0 = n_blk * kTcBN;
-  float* accp = a.acc + r * a.H + n0;
-  __nv_bfloat16* outp =
-      (tok >= 0) ? static_cast<__nv_bfloat16*>(a.dhidden) + static_cast<long long>(tok) * a.H + n0
-                 : nullptr;
+  const int lane = row & 31;
+  const int i = lane & 7;
+  const long long r_oct = r0 + (row & ~31) + (lane & ~7);
+  float* acc = a.acc + r_oct * a.H + n0;
+  // token and activity of the octet's rows p = 0..7 (row p lives in lane
+  // (lane & ~7) + p)
+  int tok_p[8];
+  uint32_t act_bits = 0;
+  if (jb.last_chunk) {
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      tok_p[p] = __shfl_sync(0xffffffffu, tok, (lane & ~7) + p);
+      if (__shfl_sync(0xffffffffu, active ? 1 : 0, (lane & ~7) + p)) act_bits |= 1u << p;
+    }
+  }
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 32; ++c) {
     if (n0 + c * 32 >= a.H) break;
@@ -264,27 +313,33 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, ui
     } else {
       tmem_ld32(tbase + c * 32, v);
     }
-    float4* ap = reinterpret_cast<float4*>(accp + c * 32);
+    octet_transpose(v, i);
     if (!jb.first_chunk) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = ap[q];
-        v[4 * q] += x.x;
-        v[4 * q + 1] += x.y;
-        v[4 * q + 2] += x.z;
-        v[4 * q + 3] += x.w;
+      for (int p = 0; p < 8; ++p) {
+        const float4 x = reinterpret_cast<const float4*>(acc + p * a.H + c * 32)[i];
+        v[4 * p] += x.x;
+        v[4 * p + 1] += x.y;
+        v[4 * p + 2] += x.z;
+        v[4 * p + 3] += x.w;
       }
     }
     if (!jb.last_chunk) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) ap[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else if (outp != nullptr) {
-      uint32_t pk[16];
+      for (int p = 0; p < 8; ++p)
+        reinterpret_cast<float4*>(acc + p * a.H + c * 32)[i] =
+            make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
+    } else {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) pk[j] = active ? pack_bf16x2(v[2 * j], v[2 * j + 1]) : 0u;
-      uint4* o = reinterpret_cast<uint4*>(outp + c * 32);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) o[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      for (int p = 0; p < 8; ++p) {
+        if (tok_p[p] < 0) continue;
+        const bool on = (act_bits >> p) & 1u;
+        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.dhidden) +
+                           static_cast<long long>(tok_p[p]) * a.H + n0 + c * 32;
+        reinterpret_cast<uint2*>(o)[i] =
+            make_uint2(on ? pack_bf16x2(v[4 * p], v[4 * p + 1]) : 0u,
+                       on ? pack_bf16x2(v[4 * p + 2], v[4 * p + 3]) : 0u);
+      }
     }
   }
 }
@@ -292,10 +347,11 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, ui
 // dW rows of this chunk: every vocabulary row of the chunk is overwritten.
 __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, uint32_t tbase,
                                             bool k_empty, long long r0, int n_blk, int row) {
-  const int m = static_cast<int>(r0) + row;
   const int n0 = n_blk * kTcBN;
-  const bool live = m < jb.vc_live;
-  float* outp = a.dW + (static_cast<long long>(jb.v0) + m) * a.H + n0;
+  const int lane = row & 31;
+  const int i = lane & 7;
+  const int m_oct = static_cast<int>(r0) + (row & ~31) + (lane & ~7);   // chunk-local vocab row
+  float* outp = a.dW + (static_cast<long long>(jb.v0) + m_oct) * a.H + n0;
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 32; ++c) {
     if (n0 + c * 32 >= a.H) break;
@@ -306,10 +362,12 @@ __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, ui
     } else {
       tmem_ld32(tbase + c * 32, v);    // warp-collective: every lane loads
     }
-    if (live) {
-      float4* o = reinterpret_cast<float4*>(outp + c * 32);
+    octet_transpose(v, i);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    for (int p = 0; p < 8; ++p) {
+      if (m_oct + p >= jb.vc_live) continue;
+      reinterpret_cast<float4*>(outp + static_cast<long long>(p) * a.H + c * 32)[i] =
+          make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
     }
   }
 }
