@@ -148,18 +148,23 @@ def _oracle_rows(inp, rows, Wf):
 def oracle_sample_size(inp, Wf, target_s: float, rng) -> int:
     """Active rows whose oracle fwd+bwd takes about target_s on this host.
 
-    The oracle's cost per row falls as batches grow (small batches are
-    memory-bound on W), so the estimate comes from a batch that already takes
-    a good fraction of a second, doubling from 8 rows."""
+    The oracle's time for a batch of n rows is close to a + b*n: a is the
+    part that does not depend on n (its passes over the fp64 copy of W, which
+    dominate small batches), b the per-row work.  Both are fitted from two
+    probe batches of 8 and 64 rows."""
     act = np.flatnonzero(inp["mask"])
-    n = 8
-    while True:
+
+    def probe(n):
         rows = np.sort(rng.choice(act, size=min(n, len(act)), replace=False))
-        t = _oracle_rows(inp, rows, Wf)
-        if t >= 0.25 * target_s or len(rows) == len(act) or n >= 1 << 20:
-            break
-        n *= 2
-    return int(max(8, min(len(act), len(rows) * target_s / max(t, 1e-9))))
+        return len(rows), _oracle_rows(inp, rows, Wf)
+
+    n1, t1 = probe(8)
+    n2, t2 = probe(64)
+    if n2 <= n1:
+        return len(act)
+    b = max((t2 - t1) / (n2 - n1), 1e-9)
+    a = max(t1 - b * n1, 0.0)
+    return int(max(8, min(len(act), (target_s - a) / b)))
 
 
 def oracle_sample_rate(inp, target_s: float):
