@@ -320,9 +320,17 @@ def main():
     dw = torch.empty((V, H), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(m=mask):
+    def step(m=mask, marks=None):
+        # marks: three timing events recorded at the step's start, after the
+        # span build and after the forward (phase split of the timed region)
+        if marks is not None:
+            marks[0].record(stream)
         eas.build_active_spans(m, args.max_gap, spans=spans, num_spans=ns, ws=sws)
+        if marks is not None:
+            marks[1].record(stream)
         eas.lmhead_fwd(hidden, weight, targets, m, spans, ns, flags, ws=ws, out=(lp, ent, lse))
+        if marks is not None:
+            marks[2].record(stream)
         # the backward reuses the row schedule and packed rows the forward
         # just left in the same workspace
         eas.lmhead_bwd(glp, gh, hidden, weight, targets, m, spans, ns, lse, ent,
@@ -333,7 +341,7 @@ def main():
         if world > 1:
             dist.barrier()
 
-    def timed(fn, k, trace=False):
+    def timed(fn, k, trace=False, marks=None):
         for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize()
@@ -343,8 +351,11 @@ def main():
         if trace:
             eas.trace_enable(True)
         e0.record(stream)
-        for _ in range(k):
-            fn()
+        for i in range(k):
+            if marks is None:
+                fn()
+            else:
+                fn(marks=marks[i])
         e1.record(stream)
         torch.cuda.synchronize()
         recs = None
@@ -365,7 +376,8 @@ def main():
 
     # ---- main timed region (device-resident inputs)
     sampler = ClockSampler(uuid) if rank == 0 else None
-    ms, recs = timed(step, args.steps, trace=True)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ms, recs = timed(step, args.steps, trace=True, marks=marks)
     clocks = sampler.stop() if sampler else None
     assert eas.read_device_status(ws) == 0 and eas.read_device_status(sws) == 0
 
@@ -396,6 +408,20 @@ def main():
                     "launches_per_step": count / args.steps,
                     "ms_per_launch": tot_ms / count}
     kernels = {k: round(v[1] / args.steps, 4) for k, v in sorted(by.items())}
+
+    # phase split of the same timed steps: span build, forward, backward
+    ends = [marks[i + 1][0] for i in range(args.steps - 1)]
+    span_ms = statistics.fmean(m[0].elapsed_time(m[1]) for m in marks)
+    fwd_ms = statistics.fmean(m[1].elapsed_time(m[2]) for m in marks)
+    bwd_ms = statistics.fmean(m[2].elapsed_time(e) for m, e in zip(marks[:-1], ends)) \
+        if args.steps > 1 else ms - span_ms - fwd_ms
+    u = 2.0 * Ta * H * V
+    phases = {"spans_ms": round(span_ms, 4), "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+              "tflops_fwd": u / (fwd_ms / 1000.0) / 1e12,
+              "tflops_bwd": 3 * u / (bwd_ms / 1000.0) / 1e12,
+              "tflops_6HV": 3 * u / (ms / 1000.0) / 1e12,
+              "note": "fwd credits 2*Ta*H*V, bwd 6*Ta*H*V (recompute, dHidden, dW); tflops_6HV "
+                      "is the whole step on 6*Ta*H*V, i.e. without crediting the recompute"}
     gemm_tflops = {k: round(kind_flops(k, Ta, H, V, args.vocab_chunk or 16384) * args.steps
                             / (v[1] / 1000.0) / 1e12, 1) for k, v in gemm.items()}
 
@@ -536,6 +562,7 @@ def main():
             "roofline": roofline,
             "kernels_ms_per_step": kernels,
             "gemm_tflops": gemm_tflops,
+            "phases": phases,
             "gpu_launches": launches,
             "dense_ablation": dense,
             "forward_only": fwd_only,
