@@ -114,8 +114,21 @@ __device__ __forceinline__ void epi_fwd(const TcArgs& a, uint32_t tbase, bool k_
     if constexpr (kScaled) {
       // e4m3 operands: z = acc * scale(row) * scale(column)
       const float* wsc = wscale + n0 + c * 32;
+      if (cvalid >= 32 && (reinterpret_cast<uintptr_t>(wsc) & 15u) == 0) {
+        // the 32 column scales as eight 16-byte loads (one line, shared by
+        // every lane of the warp)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= rscale * (j < cvalid ? __ldg(wsc + j) : 0.f);
+        for (int q = 0; q < 8; ++q) {
+          const float4 w4 = __ldg(reinterpret_cast<const float4*>(wsc) + q);
+          v[4 * q] *= rscale * w4.x;
+          v[4 * q + 1] *= rscale * w4.y;
+          v[4 * q + 2] *= rscale * w4.z;
+          v[4 * q + 3] *= rscale * w4.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] *= rscale * (j < cvalid ? __ldg(wsc + j) : 0.f);
+      }
     }
     const int tj = tgt - (n0 + c * 32);
     if (static_cast<unsigned>(tj) < static_cast<unsigned>(cvalid < 32 ? cvalid : 32)) {
