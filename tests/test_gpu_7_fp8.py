@@ -42,11 +42,62 @@ def test_fp8_forward_matches_oracle(T, H, V, w_std):
     w8, wsc = eas.quantize_rows_e4m3(w)
     spans, ns = eas.build_active_spans(m, 128)
     lp, ent, lse = eas.lmhead_fwd_fp8(h8, hs, w8, wsc, t, m, spans, ns)
-    hq = oracle.dequantize_rows_e4m3(h8.cpu().numpy(), hs.cpu().numpy())
-    wq = oracle.dequantize_rows_e4m3(w8.cpu().numpy(), wsc.cpu().numpy())
+    # the oracle quantises the host copies itself (its codes equal the
+    # device's, test_quantizer_bit_exact)
+    hq = oracle.dequantize_rows_e4m3(*oracle.quantize_rows_e4m3(W.to_f64(inp["hidden"]).astype(np.float32)))
+    wq = oracle.dequantize_rows_e4m3(*oracle.quantize_rows_e4m3(W.to_f64(inp["weight"]).astype(np.float32)))
     rlp, rent, rlse = oracle.lmhead_forward(hq, wq, inp["targets"], inp["mask"])
     assert np.max(np.abs(lp.cpu().numpy() - rlp)) <= BF16_TOL["lp"]
     assert np.max(np.abs(ent.cpu().numpy() - rent)) <= BF16_TOL["ent"]
     assert np.max(np.abs(lse.cpu().numpy() - rlse)) <= BF16_TOL["lp"]
     inactive = inp["mask"] == 0
     assert np.all(lp.cpu().numpy()[inactive] == 0)
+
+
+def test_misaligned_column_scales_give_identical_results():
+    """Column scales that start 4 bytes past a 16-byte boundary take the
+    epilogue's scalar loads; the outputs must equal the aligned call's."""
+    inp = small_inputs(600, 256, 1024, seed=44, mask_kind="bernoulli0.7", w_std=3.0)
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    h8, hs = eas.quantize_rows_e4m3(h)
+    w8, wsc = eas.quantize_rows_e4m3(w)
+    spans, ns = eas.build_active_spans(m, 128)
+    shifted = torch.empty(wsc.numel() + 1, dtype=wsc.dtype, device=wsc.device)
+    shifted[1:] = wsc
+    wsc_odd = shifted[1:]
+    assert wsc_odd.data_ptr() % 16 != 0
+    a = eas.lmhead_fwd_fp8(h8, hs, w8, wsc, t, m, spans, ns)
+    b = eas.lmhead_fwd_fp8(h8, hs, w8, wsc_odd, t, m, spans, ns)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_fp8_forward_full_size_rl_16k():
+    """The e4m3 forward at the rl_16k shape the forward-only bench line times
+    (T=16384, H=4096, V=128256), with a large-std W so the softmax is peaked;
+    sampled active rows are checked against the oracle run on operands it
+    quantised itself (about a minute of host work for W)."""
+    w = W.WORKLOADS["rl_16k"]
+    inp = W.make_inputs(w, w_std=1.5)
+    h, wt = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    h8, hs = eas.quantize_rows_e4m3(h)
+    w8, wsc = eas.quantize_rows_e4m3(wt)
+    spans, ns = eas.build_active_spans(m, 128)
+    lp, ent, lse = eas.lmhead_fwd_fp8(h8, hs, w8, wsc, t, m, spans, ns)
+    inactive = inp["mask"] == 0
+    assert np.all(lp.cpu().numpy()[inactive] == 0)
+    assert np.all(ent.cpu().numpy()[inactive] == 0)
+    act = np.flatnonzero(inp["mask"])
+    rng = np.random.default_rng(w.seed)
+    rows = np.sort(np.concatenate([act[:2], act[-2:], rng.choice(act, 60, replace=False)]))
+    rows = np.unique(rows)
+    wq = oracle.dequantize_rows_e4m3(*oracle.quantize_rows_e4m3(W.to_f64(inp["weight"]).astype(np.float32)))
+    hq = oracle.dequantize_rows_e4m3(
+        *oracle.quantize_rows_e4m3(W.to_f64(inp["hidden"][rows]).astype(np.float32)))
+    rlp, rent, rlse = oracle.lmhead_forward_rows(hq, wq, inp["targets"][rows])
+    idx = torch.from_numpy(rows).cuda()
+    assert np.max(np.abs(lp[idx].cpu().numpy() - rlp)) <= BF16_TOL["lp"]
+    assert np.max(np.abs(ent[idx].cpu().numpy() - rent)) <= BF16_TOL["ent"]
+    assert np.max(np.abs(lse[idx].cpu().numpy() - rlse)) <= BF16_TOL["lp"]
