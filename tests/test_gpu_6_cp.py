@@ -35,11 +35,11 @@ def test_cp_local_layout_and_spans(cp):
         lm, l2g = eas.cp_local_layout(m, o, cp, r)
         ref_l2g = oracle.cp_local_to_global(offs, cp, r)
         np.testing.assert_array_equal(l2g.cpu().numpy(), ref_l2g)
-        np.testing.assert_array_equal(lm.cpu().numpy(), oracle.cp_local_mask(mask, offs, cp, r))
+        ref_mask = oracle.cp_local_mask(mask, offs, cp, r)
+        np.testing.assert_array_equal(lm.cpu().numpy(), ref_mask)
         spans, ns = eas.build_active_spans(lm, 128)
         n = int(ns.item())
-        np.testing.assert_array_equal(spans[:n].cpu().numpy(),
-                                      oracle.active_spans(lm.cpu().numpy(), 128))
+        np.testing.assert_array_equal(spans[:n].cpu().numpy(), oracle.active_spans(ref_mask, 128))
 
 
 def test_invalid_layout_is_reported():
