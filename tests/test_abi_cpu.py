@@ -74,6 +74,17 @@ def test_host_side_argument_errors(libeas):
     p = 256
     assert bwd(p, p, p, p, p, p, p, p, 4, p, p, 10, 64, 100, _lib.EAS_BF16, 0, -5,
                p, p, p, 1 << 30, None) == _lib.EAS_ERR_INVALID_ARG   # vocab_chunk < 0
+    assert bwd(p, p, p, p, p, p, p, p, 4, p, p, 10, 64, 100, _lib.EAS_BF16, 0, 0,
+               p + 8, p, p, 1 << 30, None) == _lib.EAS_ERR_INVALID_ARG   # misaligned dhidden
+    assert b"align" in libeas.eas_last_error()
+    assert bwd(p, p, p, p, p, p, p, p, 4, p, p, 10, 64, 100, _lib.EAS_BF16, 0, 0,
+               p, p + 4, p, 1 << 30, None) == _lib.EAS_ERR_INVALID_ARG   # misaligned dW
+    assert bwd(p, p, p, p, p, p, p, p, 4, p, p, 10, 128, 100, _lib.EAS_E4M3, 0, 0,
+               p, p, p, 1 << 30, None) == _lib.EAS_ERR_UNSUPPORTED     # no e4m3 backward
+    assert bwd(p, p, p, p, p, p, p, p, 4, p, p, 10, 64, 100, _lib.EAS_BF16, 8, 0,
+               p, p, p, 1 << 30, None) == _lib.EAS_ERR_INVALID_ARG     # unknown flag bit
+    assert bwd(p, p, p, p, p, p, p, p, 4, p, p, 10, 64, 100, _lib.EAS_BF16, 0, 0,
+               p, p, p, 100, None) == _lib.EAS_ERR_WORKSPACE           # workspace too small
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
