@@ -33,6 +33,7 @@
 // of tile i overlap the mainloop of tile i+1.  Every mbarrier wait is bounded;
 // on expiry a CTA raises its abort flag, lets its in-flight copies and MMAs
 // land, frees TMEM and reports kStTimeout in the status word.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -897,17 +898,22 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   const int mode = family(args.jobs[0].kind);
   for (int j = 1; j < args.n_jobs; ++j)
     if (family(args.jobs[j].kind) != mode) return cudaErrorInvalidValue;
-  static bool configured[3] = {false, false, false};
+  // the large dynamic shared memory is opted into once per device and
+  // instantiation (one bit per device ordinal; a repeated opt-in is harmless)
+  static std::atomic<uint64_t> configured[3];
   void (*kern)(TcArgs) = mode == 0 ? tc_pair_kernel<0> : mode == 1 ? tc_pair_kernel<1>
                                                                     : tc_pair_kernel<2>;
   const int smem = mode == 0 ? PipeGeo<0>::kSmemBytes
                    : mode == 1 ? PipeGeo<1>::kSmemBytes
                                : PipeGeo<2>::kSmemBytes;
-  if (!configured[mode]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (bit == 0 || (configured[mode].load(std::memory_order_acquire) & bit) == 0) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured[mode] = true;
+    configured[mode].fetch_or(bit, std::memory_order_release);
   }
   const int clusters = (grid + 1) / 2;
   cudaLaunchConfig_t cfg;
