@@ -1,5 +1,5 @@
 """Seeded random sweeps of small problems against the oracle (the full
-path, the e4m3 forward, and vocabulary shards).
+path, the e4m3 forward, vocabulary shards and context-parallel layouts).
 
 Each case draws its dtype, hidden width, token count, vocabulary size,
 vocabulary chunk (including widths that are not multiples of the 256-column
@@ -116,3 +116,27 @@ def test_random_vocab_shards_match_oracle(i):
     assert rel_fro(dh_sum.cpu().numpy(), rdh) <= tol["fro"]
     assert rel_fro(torch.cat(dws).cpu().numpy(), rdw) <= tol["fro"]
     assert torch.all(dh_sum[torch.from_numpy(inp["mask"] == 0).cuda()] == 0)
+
+
+@pytest.mark.parametrize("i", range(20))
+def test_random_cp_layouts_match_oracle(i):
+    """Random packed layouts (1-40 segments, CP sizes 1-8, mask densities
+    from 5 to 95 %): every rank's local order, local mask and CP-local spans
+    bit for bit against the oracle."""
+    rng = np.random.default_rng(6000 + i)
+    cp = int(rng.choice([1, 2, 3, 4, 8]))
+    n_segs = int(rng.integers(1, 41))
+    lens = rng.integers(1, 20, size=n_segs) * 2 * cp
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    T = int(offs[-1])
+    mask = (rng.random(T) < rng.uniform(0.05, 0.95)).astype(np.uint8)
+    m, o = to_dev(mask), to_dev(offs)
+    gap = int(rng.choice([0, 3, 128]))
+    for r in range(cp):
+        lm, l2g = eas.cp_local_layout(m, o, cp, r)
+        np.testing.assert_array_equal(l2g.cpu().numpy(), oracle.cp_local_to_global(offs, cp, r))
+        ref_mask = oracle.cp_local_mask(mask, offs, cp, r)
+        np.testing.assert_array_equal(lm.cpu().numpy(), ref_mask)
+        spans, ns = eas.build_active_spans(lm, gap)
+        n = int(ns.item())
+        np.testing.assert_array_equal(spans[:n].cpu().numpy(), oracle.active_spans(ref_mask, gap))
