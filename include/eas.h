@@ -61,7 +61,7 @@ typedef enum {
     EAS_ERR_INVALID_ARG = 1,    /* a host-visible argument is wrong            */
     EAS_ERR_INVALID_SPANS = 2,  /* spans unsorted, out of range, overlapping,
                                    or an active token lies outside every span */
-    EAS_ERR_UNSUPPORTED = 3,    /* shape or alignment this build does not run  */
+    EAS_ERR_UNSUPPORTED = 3,    /* shape or alignment the library does not run */
     EAS_ERR_WORKSPACE = 4,      /* workspace missing or smaller than required */
     EAS_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed           */
     EAS_ERR_TIMEOUT = 6,        /* a kernel pipeline wait ran out of time      */
