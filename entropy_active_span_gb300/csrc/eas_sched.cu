@@ -314,6 +314,42 @@ __device__ __forceinline__ void lse_merge(Lse3& a, float m, float s, float u) {
     a.u += f * (u + d * s);
   }
 }
+// Group g's fold of packed row r over the tiles n = g, g + 8, g + 16, ...
+// Four accumulators take every fourth of those tiles, so four tiles' loads
+// are in flight at once, and merge in a fixed order at the end.
+__device__ __forceinline__ Lse3 fold_tiles(const float* __restrict__ pm,
+                                           const float* __restrict__ ps,
+                                           const float* __restrict__ pu, int n_tiles,
+                                           long long stride, int r, int g) {
+  Lse3 a[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) a[j] = Lse3{0.f, 0.f, 0.f};
+  int n = g;
+  for (; n + 3 * kCombGroups < n_tiles; n += 4 * kCombGroups) {
+    float m[4], sv[4], u[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long o = static_cast<long long>(n + j * kCombGroups) * stride + r;
+      m[j] = pm[o];
+      sv[j] = ps[o];
+      u[j] = pu[o];
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) lse_merge(a[j], m[j], sv[j], u[j]);
+  }
+  // at most three tiles remain
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    if (n < n_tiles) {
+      const long long o = static_cast<long long>(n) * stride + r;
+      lse_merge(a[j], pm[o], ps[o], pu[o]);
+      n += kCombGroups;
+    }
+  }
+#pragma unroll
+  for (int j = 1; j < 4; ++j) lse_merge(a[0], a[j].m, a[j].s, a[j].u);
+  return a[0];
+}
 }  // namespace
 
 __global__ void __launch_bounds__(kCombTok * kCombGroups)
@@ -333,12 +369,7 @@ combine_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
       if (r >= 0 && mask[t] == 0) r = -1;
     }
     Lse3 a{0.f, 0.f, 0.f};
-    if (r >= 0) {
-      for (int n = g; n < n_tiles; n += kCombGroups) {
-        const long long o = n * stride + r;
-        lse_merge(a, pm[o], ps[o], pu[o]);
-      }
-    }
+    if (r >= 0) a = fold_tiles(pm, ps, pu, n_tiles, stride, r, g);
     st[g][x] = a;
     __syncthreads();
     if (g == 0 && t < T) {
@@ -381,12 +412,7 @@ combine_stats_kernel(const float* __restrict__ pm, const float* __restrict__ ps,
       if (r >= 0 && mask[t] == 0) r = -1;
     }
     Lse3 a{0.f, 0.f, 0.f};
-    if (r >= 0) {
-      for (int n = g; n < n_tiles; n += kCombGroups) {
-        const long long o = n * stride + r;
-        lse_merge(a, pm[o], ps[o], pu[o]);
-      }
-    }
+    if (r >= 0) a = fold_tiles(pm, ps, pu, n_tiles, stride, r, g);
     st[g][x] = a;
     __syncthreads();
     if (g == 0 && t < T) {
