@@ -141,6 +141,22 @@ def test_active_rows_independent_of_row_policy():
         np.testing.assert_array_equal(a[k], b[k])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_active_rows_match_the_dense_mask_run(dtype):
+    """A sparse mask's active rows get bit-identical forward outputs and
+    dHidden rows to the same rows in a run where every token is active: each
+    row's arithmetic depends only on that row and the vocabulary tiling, not
+    on which other rows share its tile."""
+    inp = small_inputs(900, 256 if dtype == "bf16" else 36, 1500, dtype=dtype, seed=31,
+                       mask_kind="bernoulli0.4", w_std=3.0)
+    sparse = run_gpu(inp, vocab_chunk=512)
+    dense_inp = dict(inp, mask=np.ones_like(inp["mask"]))
+    dense = run_gpu(dense_inp, vocab_chunk=512)
+    act = inp["mask"] != 0
+    for k in ("logprob", "entropy", "lse", "dhidden"):
+        np.testing.assert_array_equal(sparse[k][act], dense[k][act])
+
+
 @pytest.mark.parametrize("T,H,V", [(300, 192, 300), (513, 320, 1000), (1, 64, 50), (257, 448, 2049)])
 def test_bf16_hidden_width_not_a_tile_multiple(T, H, V):
     """H % 256 != 0 leaves a partial N tile in dHidden and dW; T = 1 is a
