@@ -47,6 +47,25 @@ def test_exhaustive_small_masks():
                 np.testing.assert_array_equal(got, ref.reshape(-1, 2))
 
 
+@pytest.mark.parametrize("T", [10, 12, 14, 16])
+@pytest.mark.parametrize("g", [0, 1, 2, 3, 5, 128])
+def test_exhaustive_masks_in_one_call(T, g):
+    """Every mask of T tokens at once: the 2^T masks laid end to end, each
+    followed by g + 1 inactive tokens so that no span can join two of them.
+    The spans of the whole are then each mask's own spans, offset by the
+    mask's position."""
+    n_masks = 1 << T
+    stride = T + g + 1
+    bits = ((np.arange(n_masks)[:, None] >> np.arange(T)[None, :]) & 1).astype(np.uint8)
+    whole = np.zeros((n_masks, stride), np.uint8)
+    whole[:, :T] = bits
+    got, n = gpu_spans(whole.reshape(-1), g)
+    ref = [active_spans(bits[k], g).reshape(-1, 2) + k * stride for k in range(n_masks)]
+    ref = np.concatenate([r for r in ref if len(r)] or [np.zeros((0, 2), np.int64)])
+    assert n == len(ref)
+    np.testing.assert_array_equal(got, ref)
+
+
 @pytest.mark.parametrize("name", list(W.WORKLOADS))
 @pytest.mark.parametrize("g", [0, 128])
 def test_workload_masks_match_golden(name, g):
