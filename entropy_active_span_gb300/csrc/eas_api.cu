@@ -11,6 +11,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <deque>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/eas.h"
@@ -113,7 +114,7 @@ struct TraceRec {
 };
 
 std::mutex g_trace_mu;
-bool g_trace_on = false;
+std::atomic<bool> g_trace_on{false};   // read unlocked on every launch
 std::deque<TraceRec> g_trace_pool;    // events are created once and reused; a deque
                                       // keeps records in place as it grows
 size_t g_trace_used = 0;
@@ -121,11 +122,16 @@ size_t g_trace_used = 0;
 class Trace {
  public:
   Trace(int kind, cudaStream_t s) : s_(s) {
-    if (!g_trace_on) return;
+    if (!g_trace_on.load(std::memory_order_relaxed)) return;
     std::lock_guard<std::mutex> lk(g_trace_mu);
+    if (!g_trace_on.load(std::memory_order_relaxed)) return;
     if (g_trace_used == g_trace_pool.size()) {
       TraceRec r{kind, nullptr, nullptr};
-      if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+      if (cudaEventCreate(&r.a) != cudaSuccess) return;
+      if (cudaEventCreate(&r.b) != cudaSuccess) {
+        cudaEventDestroy(r.a);
+        return;
+      }
       g_trace_pool.push_back(r);
     }
     rec_ = &g_trace_pool[g_trace_used++];
@@ -854,8 +860,8 @@ eas_status eas_read_device_status(const void* ws, void* stream) {
 
 void eas_trace_enable(int32_t on) {
   std::lock_guard<std::mutex> lk(g_trace_mu);
-  g_trace_on = (on != 0);
-  if (g_trace_on) g_trace_used = 0;
+  g_trace_on.store(on != 0, std::memory_order_relaxed);
+  if (on != 0) g_trace_used = 0;
 }
 
 int32_t eas_trace_read(int32_t* kinds, float* ms, int32_t cap) {

@@ -344,7 +344,9 @@ eas_status eas_selftest_wait_timeout(int64_t budget_cycles, void* ws, size_t ws_
  * eas_trace_read() waits for the recorded events and writes, for the first
  * min(n, cap) launches, the kernel kind (see eas_kernel_name) and its
  * duration in milliseconds; it returns n, the number of recorded launches.
- * For eager launches only (not inside a CUDA graph capture).
+ * For eager launches only (not inside a CUDA graph capture).  The trace is
+ * process-wide: launches from every host thread and device are recorded
+ * into the one list, in the order they were issued.
  */
 void eas_trace_enable(int32_t on);
 int32_t eas_trace_read(int32_t* kinds, float* ms, int32_t cap);
