@@ -3,15 +3,22 @@
 
 One step = the whole hot path over one batch: active spans built on the device
 from the loss mask, the fused forward (target logprob, entropy, lse of the
-active tokens) and the backward (d-logits of active tiles, dHidden, dW), on
-the synthetic rl_16k workload by default (T=16384 tokens, H=4096, V=128256,
-bf16; 16 sequences of 1024 tokens whose first 256..512 prompt tokens are
-inactive).  Metric: active tokens per second of fwd+bwd, and the fraction of
-the GB300 dense-bf16 tensor peak achieved on active FLOPs (8 * Ta * H * V per
-step: forward logits, backward recompute, dHidden and dW, each 2 * Ta * H * V).
+active tokens) and the backward (d-logits of active tiles, dHidden, dW).  The
+default workload is the largest one-GPU configuration, long_256k (T=262144
+tokens, H=8192, V=128256, bf16; 32 sequences of 8192 tokens whose first
+2458..4096 prompt tokens are inactive, about 60 % active), with its dense-mask
+ablation (every token active) timed alongside.  rl_16k (T=16384, H=4096,
+V=128256) is timed as a secondary line inside the same JSON.  Metric: active
+tokens per second of fwd+bwd, and the fraction of the GB300 dense-bf16 tensor
+peak achieved on active FLOPs (8 * Ta * H * V per step: forward logits,
+backward recompute, dHidden and dW, each 2 * Ta * H * V).  Every fraction is
+given against four denominators: the measured sustained and burst cuBLAS bf16
+rates, the nominal dense-bf16 peak (2250 TFLOP/s), and the tensor peak at the
+SM clock sampled during that timed region (SMs x 8192 flop/clk x MHz).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload rl_16k] [--max-gap 128] [--vocab-chunk 0]
+                    [--workload long_256k] [--secondary rl_16k|none]
+                    [--max-gap 128] [--vocab-chunk 0]
 
 Prints one JSON line on rank 0.  --impl reference times the CPU oracle (fp64
 NumPy) on a bounded sample of the same workload.
@@ -36,6 +43,8 @@ from entropy_active_span_gb300 import workloads as W  # noqa: E402
 
 METRIC = "active tokens/sec fwd+bwd; % of GB300 bf16 tensor peak on active FLOPs"
 UNIT = "active tokens/s"
+NOMINAL_BF16_TFLOPS = 2250.0     # GB300 dense bf16, nominal
+FLOP_PER_CLK_SM = 8192           # dense bf16 tensor flop per SM per clock (tcgen05)
 GEMM_KINDS = ("fwd_gemm_tc", "dlogits_gemm_tc", "bwd_chunk_gemm_tc", "dproj_gemm_tc")
 
 
@@ -67,7 +76,12 @@ def parse_args():
     p.add_argument("--steps", type=int, default=40)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default="rl_16k", choices=sorted(W.ALL_WORKLOADS))
+    p.add_argument("--workload", default="long_256k", choices=sorted(W.ALL_WORKLOADS))
+    p.add_argument("--secondary", default="rl_16k",
+                   help="workload timed as a secondary line ('none' to skip)")
+    p.add_argument("--ablation-steps", type=int, default=10,
+                   help="timed steps of the dense, forward-only and secondary passes "
+                        "(at most --steps)")
     p.add_argument("--max-gap", type=int, default=128)
     p.add_argument("--vocab-chunk", type=int, default=0)
     p.add_argument("--rows", choices=("active", "span"), default="active")
@@ -91,24 +105,47 @@ def peaks():
     return dict(bf16=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary, or None.
+def fractions(tflops: float, pk: dict, sm_mhz, sms: int, peak_scale: float = 1.0) -> dict:
+    """`tflops` against the four denominators.  peak_scale multiplies every
+    bf16 peak (2 for e4m3 operands: the nominal dense fp8/bf16 ratio)."""
+    out = {"frac_sustained": tflops / (peak_scale * pk["bf16_sustained"]),
+           "frac_burst": tflops / (peak_scale * pk["bf16"]),
+           "frac_nominal": tflops / (peak_scale * NOMINAL_BF16_TFLOPS),
+           "frac_per_clock": None, "per_clock_peak_tflops": None, "sm_mhz_median": sm_mhz}
+    if sm_mhz:
+        pc = peak_scale * sms * FLOP_PER_CLK_SM * sm_mhz * 1e6 / 1e12
+        out["per_clock_peak_tflops"] = pc
+        out["frac_per_clock"] = tflops / pc
+    return out
 
-    Summaries under profiles/ carry lines 'traffic <kernel> <bytes> <sha>'
-    where sha is sha256[:16] of the tensor-core kernel sources at capture
-    time; a figure taken from an older kernel is not reported."""
-    import glob
+
+def source_sha() -> str:
+    """sha256[:16] of the tensor-core kernel sources (identifies a capture's kernel)."""
     import hashlib
     csrc = os.path.join(ROOT, "entropy_active_span_gb300", "csrc")
     src = "".join(open(os.path.join(csrc, f)).read()
                   for f in ("eas_gemm_tc.cu", "eas_device.cuh", "eas_kernels.h"))
-    sha = hashlib.sha256(src.encode()).hexdigest()[:16]
+    return hashlib.sha256(src.encode()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, shape: str):
+    """DRAM bytes per launch of `kernel` at launch shape `shape` (a workload
+    name and its vocabulary chunk, e.g. 'long_256k/c16384') from a committed
+    ncu summary, with that summary's file name; (None, None) if there is none.
+
+    Summaries under profiles/ carry lines 'traffic <kernel> <shape> <bytes>
+    <sha>', where sha is source_sha() at capture time: a figure taken from
+    another kernel build, another launch shape or another workload is never
+    reported."""
+    import glob
+    sha = source_sha()
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(path):
             parts = line.split()
-            if len(parts) == 4 and parts[0] == "traffic" and parts[1] == kernel and parts[3] == sha:
-                return int(parts[2])
-    return None
+            if (len(parts) == 5 and parts[0] == "traffic" and parts[1] == kernel
+                    and parts[2] == shape and parts[4] == sha):
+                return int(parts[3]), os.path.basename(path)
+    return None, None
 
 
 def aggregate_ranks(ms: float, tokens: float, device) -> tuple[float, float]:
@@ -275,6 +312,66 @@ class ClockSampler:
 
 # -------------------------------------------------------------- our arm
 
+class Problem:
+    """Device-resident inputs, outputs and workspaces of one workload."""
+
+    def __init__(self, w, rank, args, dev, eas):
+        import torch
+        self.w = w
+        wr = w.replace(seed=w.seed + 1000 * rank)     # each rank: its own batch (weak scaling)
+        self.inp = W.make_inputs(wr)
+        self.T, self.H, self.V = w.T, w.H, w.V
+        self.Ta = int(self.inp["mask"].sum())
+        self.flags = eas.EAS_ROWS_SPAN if args.rows == "span" else eas.EAS_ROWS_ACTIVE
+        self.args, self.dev, self.eas = args, dev, eas
+        T, H, V = self.T, self.H, self.V
+
+        def d(x):
+            t = torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+            return t.view(torch.bfloat16) if x.dtype == np.uint16 else t
+
+        inp = self.inp
+        self.hidden, self.weight = d(inp["hidden"]), d(inp["weight"])
+        self.targets, self.mask = d(inp["targets"]), d(inp["mask"])
+        self.glp, self.gh = d(inp["g_logprob"]), d(inp["g_entropy"])
+        cap = (T + 1) // 2
+        self.spans = torch.empty((cap, 2), dtype=torch.int32, device=dev)
+        self.ns = torch.empty(1, dtype=torch.int32, device=dev)
+        self.sws = eas.workspace(eas.spans_workspace_size(T), dev)
+        self.ws_bytes = eas.lmhead_workspace_size(T, H, V, torch.bfloat16, args.vocab_chunk)
+        self.ws = eas.workspace(self.ws_bytes, dev)
+        self.lp, self.ent, self.lse = (torch.empty(T, dtype=torch.float32, device=dev)
+                                       for _ in range(3))
+        self.dh = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        self.dw = torch.empty((V, H), dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def step(self, m=None, marks=None, d_in=None):
+        """One pass of the hot path.  marks: three timing events recorded at
+        the step's start, after the span build and after the forward (phase
+        split of the timed region).  d_in: other device inputs (end to end)."""
+        eas, a = self.eas, self.args
+        x = d_in or {"hidden": self.hidden, "weight": self.weight, "targets": self.targets,
+                     "mask": self.mask if m is None else m, "g_logprob": self.glp,
+                     "g_entropy": self.gh}
+        if marks is not None:
+            marks[0].record(self.stream)
+        eas.build_active_spans(x["mask"], a.max_gap, spans=self.spans, num_spans=self.ns,
+                               ws=self.sws)
+        if marks is not None:
+            marks[1].record(self.stream)
+        eas.lmhead_fwd(x["hidden"], x["weight"], x["targets"], x["mask"], self.spans, self.ns,
+                       self.flags, ws=self.ws, out=(self.lp, self.ent, self.lse))
+        if marks is not None:
+            marks[2].record(self.stream)
+        # the backward reuses the row schedule and packed rows the forward
+        # just left in the same workspace
+        eas.lmhead_bwd(x["g_logprob"], x["g_entropy"], x["hidden"], x["weight"], x["targets"],
+                       x["mask"], self.spans, self.ns, self.lse, self.ent,
+                       self.flags | eas.EAS_REUSE_FWD_ROWS, a.vocab_chunk, ws=self.ws,
+                       dhidden=self.dh, dweight=self.dw)
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -297,56 +394,31 @@ def main():
     w = W.ALL_WORKLOADS[args.workload]
     if w.dtype != "bf16":
         raise SystemExit("bench measures the bf16 tensor-core path")
-    wr = w.replace(seed=w.seed + 1000 * rank)     # each rank: its own batch (weak scaling)
-    inp = W.make_inputs(wr)
-    T, H, V = w.T, w.H, w.V
-    Ta = int(inp["mask"].sum())
-    flags = eas.EAS_ROWS_SPAN if args.rows == "span" else eas.EAS_ROWS_ACTIVE
-
-    def d(x):
-        t = torch.from_numpy(np.ascontiguousarray(x)).to(dev)
-        return t.view(torch.bfloat16) if x.dtype == np.uint16 else t
-
-    hidden, weight = d(inp["hidden"]), d(inp["weight"])
-    targets, mask = d(inp["targets"]), d(inp["mask"])
-    glp, gh = d(inp["g_logprob"]), d(inp["g_entropy"])
-    cap = (T + 1) // 2
-    spans = torch.empty((cap, 2), dtype=torch.int32, device=dev)
-    ns = torch.empty(1, dtype=torch.int32, device=dev)
-    sws = eas.workspace(eas.spans_workspace_size(T), dev)
-    ws = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.bfloat16, args.vocab_chunk), dev)
-    lp, ent, lse = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
-    dh = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
-    dw = torch.empty((V, H), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step(m=mask, marks=None):
-        # marks: three timing events recorded at the step's start, after the
-        # span build and after the forward (phase split of the timed region)
-        if marks is not None:
-            marks[0].record(stream)
-        eas.build_active_spans(m, args.max_gap, spans=spans, num_spans=ns, ws=sws)
-        if marks is not None:
-            marks[1].record(stream)
-        eas.lmhead_fwd(hidden, weight, targets, m, spans, ns, flags, ws=ws, out=(lp, ent, lse))
-        if marks is not None:
-            marks[2].record(stream)
-        # the backward reuses the row schedule and packed rows the forward
-        # just left in the same workspace
-        eas.lmhead_bwd(glp, gh, hidden, weight, targets, m, spans, ns, lse, ent,
-                       flags | eas.EAS_REUSE_FWD_ROWS, args.vocab_chunk, ws=ws, dhidden=dh,
-                       dweight=dw)
+    abl_steps = max(1, min(args.steps, args.ablation_steps))
+    chunk = args.vocab_chunk or 16384
+    pk = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    uuid = None
+    try:
+        uuid = str(props.uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        uuid = None
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    def timed(fn, k, trace=False, marks=None):
+    def timed(fn, k, stream, trace=False, marks=None, clocks=True):
+        """Warm-up, then k timed calls bracketed by barrier + synchronize;
+        returns (ms per call over the slowest rank, trace records, clocks)."""
         for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
+        sampler = ClockSampler(uuid) if (clocks and rank == 0) else None
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if trace:
             eas.trace_enable(True)
@@ -358,6 +430,7 @@ def main():
                 fn(marks=marks[i])
         e1.record(stream)
         torch.cuda.synchronize()
+        clk = sampler.stop() if sampler else None
         recs = None
         if trace:
             eas.trace_enable(False)
@@ -365,49 +438,73 @@ def main():
         barrier()
         torch.cuda.synchronize()
         ms, _ = aggregate_ranks(e0.elapsed_time(e1), 0.0, dev)
-        return ms / k, recs
+        return ms / k, recs, clk
 
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-    except Exception:
-        uuid = None
+    def mhz(clk):
+        return clk["sm_mhz"] if clk else None
 
-    # ---- main timed region (device-resident inputs)
-    sampler = ClockSampler(uuid) if rank == 0 else None
+    def rate_block(tflops, clk, peak_scale=1.0):
+        f = fractions(tflops, pk, mhz(clk), sms, peak_scale)
+        return {"tflops": tflops, "frac_of_peak": f["frac_sustained"],
+                "frac_of_burst": f["frac_burst"], "frac_of_nominal": f["frac_nominal"],
+                "frac_per_clock": f["frac_per_clock"], "sm_mhz_median": f["sm_mhz_median"],
+                "power_w_median": clk.get("power_w_median") if clk else None}
+
+    def breakdown(P, recs, steps, ms, clk):
+        """Per-kernel times from the library's event trace, the roofline of
+        the dominant tensor-core launch kind, and the launch count."""
+        by = {}
+        for name, t in recs:
+            e = by.setdefault(name, [0, 0.0])
+            e[0] += 1
+            e[1] += t
+        launches = sum(c for n, (c, _) in by.items() if n != "memset")
+        gemm = {k: v for k, v in by.items() if k in GEMM_KINDS}
+        top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
+        roofline = None
+        if top is not None:
+            name, (count, tot_ms) = top
+            flops_kind = kind_flops(name, P.Ta, P.H, P.V, chunk) * steps
+            achieved = flops_kind / (tot_ms / 1000.0) / 1e12
+            f = fractions(achieved, pk, mhz(clk), sms)
+            shape = f"{P.w.name}/c{chunk}" + ("/span" if args.rows == "span" else "")
+            traffic, tsrc = recorded_traffic(name, shape)
+            roofline = {"bound": "tensor", "kernel": name, "achieved": achieved,
+                        "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                        "frac": achieved / pk["bf16_sustained"],
+                        "peak_kind": f"bf16_tflops_sustained ({pk['source']}): the kernel runs "
+                                     "inside a seconds-long, power-capped step",
+                        "frac_burst": f["frac_burst"], "peak_burst": pk["bf16"],
+                        "frac_nominal": f["frac_nominal"], "peak_nominal": NOMINAL_BF16_TFLOPS,
+                        "frac_per_clock": f["frac_per_clock"],
+                        "peak_per_clock": f["per_clock_peak_tflops"],
+                        "sm_mhz_median": f["sm_mhz_median"],
+                        "per_clock_rule": f"{sms} SMs x {FLOP_PER_CLK_SM} flop/clk x median "
+                                          "SM MHz sampled during this timed region",
+                        "traffic": traffic, "traffic_shape": shape,
+                        "traffic_source": (f"profiles/{tsrc}" if tsrc else
+                                           "no capture of this kernel build at this launch "
+                                           "shape"),
+                        "algorithmic_flops_per_launch": flops_kind / count,
+                        "launches_per_step": count / steps,
+                        "ms_per_launch": tot_ms / count}
+        kernels = {k: round(v[1] / steps, 4) for k, v in sorted(by.items())}
+        gemm_tflops = {k: round(kind_flops(k, P.Ta, P.H, P.V, chunk) * steps
+                                / (v[1] / 1000.0) / 1e12, 1) for k, v in gemm.items()}
+        return roofline, kernels, gemm_tflops, launches
+
+    # ---- headline workload: main timed region (device-resident inputs)
+    P = Problem(w, rank, args, dev, eas)
+    T, H, V, Ta = P.T, P.H, P.V, P.Ta
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    ms, recs = timed(step, args.steps, trace=True, marks=marks)
-    clocks = sampler.stop() if sampler else None
-    assert eas.read_device_status(ws) == 0 and eas.read_device_status(sws) == 0
+    ms, recs, clocks = timed(P.step, args.steps, P.stream, trace=True, marks=marks)
+    assert eas.read_device_status(P.ws) == 0 and eas.read_device_status(P.sws) == 0
 
     _, tokens_all = aggregate_ranks(0.0, float(Ta), dev)
     value = tokens_all / (ms / 1000.0)
-    pk = peaks()
     flops_step = 8.0 * Ta * H * V
     tflops = flops_step / (ms / 1000.0) / 1e12
-
-    # per-kernel breakdown from the library's event trace
-    by = {}
-    for name, t in recs:
-        e = by.setdefault(name, [0, 0.0])
-        e[0] += 1
-        e[1] += t
-    launches = sum(c for n, (c, _) in by.items() if n != "memset")
-    gemm = {k: v for k, v in by.items() if k in GEMM_KINDS}
-    top = max(gemm.items(), key=lambda kv: kv[1][1]) if gemm else None
-    roofline = None
-    if top is not None:
-        name, (count, tot_ms) = top
-        flops_kind = kind_flops(name, Ta, H, V, args.vocab_chunk or 16384) * args.steps
-        achieved = flops_kind / (tot_ms / 1000.0) / 1e12
-        roofline = {"bound": "tensor", "kernel": name, "achieved": achieved,
-                    "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": achieved / pk["bf16_sustained"], "traffic": recorded_traffic(name),
-                    "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
-                    "launches_per_step": count / args.steps,
-                    "ms_per_launch": tot_ms / count}
-    kernels = {k: round(v[1] / args.steps, 4) for k, v in sorted(by.items())}
+    roofline, kernels, gemm_tflops, launches = breakdown(P, recs, args.steps, ms, clocks)
 
     # phase split of the same timed steps: span build, forward, backward
     ends = [marks[i + 1][0] for i in range(args.steps - 1)]
@@ -422,8 +519,6 @@ def main():
               "tflops_6HV": 3 * u / (ms / 1000.0) / 1e12,
               "note": "fwd credits 2*Ta*H*V, bwd 6*Ta*H*V (recompute, dHidden, dW); tflops_6HV "
                       "is the whole step on 6*Ta*H*V, i.e. without crediting the recompute"}
-    gemm_tflops = {k: round(kind_flops(k, Ta, H, V, args.vocab_chunk or 16384) * args.steps
-                            / (v[1] / 1000.0) / 1e12, 1) for k, v in gemm.items()}
 
     # ---- end to end: host (pinned) inputs in, results out, through the API.
     # Measured right after the main timed region, before the ablations below,
@@ -436,17 +531,16 @@ def main():
     e2e = None
     if not args.no_e2e:
         names = ("hidden", "weight", "targets", "mask", "g_logprob", "g_entropy")
-        host = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).pin_memory() for k in names}
-        bufs = [{"hidden": hidden, "weight": weight, "targets": targets, "mask": mask,
-                 "g_logprob": glp, "g_entropy": gh},
-                {k: torch.empty_like(v) for k, v in (("hidden", hidden), ("weight", weight),
-                                                      ("targets", targets), ("mask", mask),
-                                                      ("g_logprob", glp), ("g_entropy", gh))}]
+        host = {k: torch.from_numpy(np.ascontiguousarray(P.inp[k])).pin_memory() for k in names}
+        first = {"hidden": P.hidden, "weight": P.weight, "targets": P.targets, "mask": P.mask,
+                 "g_logprob": P.glp, "g_entropy": P.gh}
+        bufs = [first, {k: torch.empty_like(v) for k, v in first.items()}]
         out_lp = torch.empty(T, dtype=torch.float32).pin_memory()
         out_ent = torch.empty(T, dtype=torch.float32).pin_memory()
         copy_stream = torch.cuda.Stream(dev)
         ready = [torch.cuda.Event() for _ in range(2)]
         free = [torch.cuda.Event() for _ in range(2)]
+        stream = P.stream
 
         def run_e2e(k, start_event=None):
             for i in range(k):
@@ -461,17 +555,10 @@ def main():
                             host[name].view(torch.uint8).view(-1), non_blocking=True)
                     ready[b].record(copy_stream)
                 stream.wait_event(ready[b])
-                d_in = bufs[b]
-                eas.build_active_spans(d_in["mask"], args.max_gap, spans=spans, num_spans=ns, ws=sws)
-                eas.lmhead_fwd(d_in["hidden"], d_in["weight"], d_in["targets"], d_in["mask"],
-                               spans, ns, flags, ws=ws, out=(lp, ent, lse))
-                eas.lmhead_bwd(d_in["g_logprob"], d_in["g_entropy"], d_in["hidden"],
-                               d_in["weight"], d_in["targets"], d_in["mask"], spans, ns, lse, ent,
-                               flags | eas.EAS_REUSE_FWD_ROWS, args.vocab_chunk, ws=ws,
-                               dhidden=dh, dweight=dw)
+                P.step(d_in=bufs[b])
                 free[b].record(stream)
-                out_lp.copy_(lp, non_blocking=True)
-                out_ent.copy_(ent, non_blocking=True)
+                out_lp.copy_(P.lp, non_blocking=True)
+                out_ent.copy_(P.ent, non_blocking=True)
 
         run_e2e(args.warmup)
         torch.cuda.synchronize()
@@ -494,16 +581,21 @@ def main():
                        "pinned host memory and reads logprob and entropy back; step i+1's "
                        "inputs are copied on a second stream while step i computes; "
                        "gradients stay on the device"}
-        del bufs
+        del bufs, host
 
-    # ---- dense-mask ablation (same kernels, every token active)
+    # ---- dense-mask ablation (same kernels, every token active): the
+    # skip-vs-dense comparison of the same workload
     dense = None
     if not args.no_dense:
         ones = torch.ones(T, dtype=torch.uint8, device=dev)
-        dms, _ = timed(lambda: step(ones), args.steps)
-        dense = {"ms_per_step": dms, "active_tokens_per_s": world * T / (dms / 1000.0),
-                 "tflops": 8.0 * T * H * V / (dms / 1000.0) / 1e12,
-                 "frac_of_peak": 8.0 * T * H * V / (dms / 1000.0) / 1e12 / pk["bf16_sustained"]}
+        dms, _, dclk = timed(lambda: P.step(ones), abl_steps, P.stream)
+        dense = {"ms_per_step": dms, "steps": abl_steps,
+                 "active_tokens_per_s": world * T / (dms / 1000.0),
+                 **rate_block(8.0 * T * H * V / (dms / 1000.0) / 1e12, dclk),
+                 "skip_speedup": dms / ms,
+                 "note": "all T tokens active; ms_per_step / the sparse step's is what skipping "
+                         "the inactive tokens saves"}
+        del ones
 
     # ---- forward-only scoring (no lse kept): bf16 operands, and e4m3 operands
     # with W quantised once and hidden quantised inside every step
@@ -512,41 +604,65 @@ def main():
         ws_fwd = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.bfloat16), dev)
 
         def score_bf16():
-            eas.build_active_spans(mask, args.max_gap, spans=spans, num_spans=ns, ws=sws)
-            eas.lmhead_fwd(hidden, weight, targets, mask, spans, ns, flags, ws=ws_fwd,
-                           out=(lp, ent, lse), want_lse=False)
+            eas.build_active_spans(P.mask, args.max_gap, spans=P.spans, num_spans=P.ns,
+                                   ws=P.sws)
+            eas.lmhead_fwd(P.hidden, P.weight, P.targets, P.mask, P.spans, P.ns, P.flags,
+                           ws=ws_fwd, out=(P.lp, P.ent, P.lse), want_lse=False)
 
-        w8, wsc = eas.quantize_rows_e4m3(weight)
+        w8, wsc = eas.quantize_rows_e4m3(P.weight)
         h8 = torch.empty((T, H), dtype=torch.uint8, device=dev)
         hsc = torch.empty(T, dtype=torch.float32, device=dev)
         ws8 = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.uint8), dev)
 
         def score_fp8():
-            eas.quantize_rows_e4m3(hidden, out=h8, scale=hsc)
-            eas.build_active_spans(mask, args.max_gap, spans=spans, num_spans=ns, ws=sws)
-            eas.lmhead_fwd_fp8(h8, hsc, w8, wsc, targets, mask, spans, ns, flags, ws=ws8,
-                               out=(lp, ent, lse), want_lse=False)
+            eas.quantize_rows_e4m3(P.hidden, out=h8, scale=hsc)
+            eas.build_active_spans(P.mask, args.max_gap, spans=P.spans, num_spans=P.ns,
+                                   ws=P.sws)
+            eas.lmhead_fwd_fp8(h8, hsc, w8, wsc, P.targets, P.mask, P.spans, P.ns, P.flags,
+                               ws=ws8, out=(P.lp, P.ent, P.lse), want_lse=False)
 
         fwd_only = {}
-        for name, fn, peak in (("bf16", score_bf16, pk["bf16_sustained"]),
-                               ("e4m3", score_fp8, 2.0 * pk["bf16_sustained"])):
-            fms, _ = timed(fn, args.steps)
+        for name, fn, scale in (("bf16", score_bf16, 1.0), ("e4m3", score_fp8, 2.0)):
+            fms, _, fclk = timed(fn, abl_steps, P.stream)
             tf = 2.0 * Ta * H * V / (fms / 1000.0) / 1e12
-            fwd_only[name] = {"ms_per_step": fms, "active_tokens_per_s": tokens_all / (fms / 1000.0),
-                              "tflops": tf, "peak_tflops": peak, "frac_of_peak": tf / peak}
-        fwd_only["e4m3"]["peak_kind"] = ("bf16_tflops_sustained x 2 (nominal dense fp8/bf16 "
+            fwd_only[name] = {"ms_per_step": fms, "steps": abl_steps,
+                              "active_tokens_per_s": tokens_all / (fms / 1000.0),
+                              **rate_block(tf, fclk, scale)}
+        fwd_only["e4m3"]["peak_kind"] = ("every bf16 denominator x 2 (nominal dense fp8/bf16 "
                                          "ratio 4.5/2.25)")
         del ws_fwd, ws8, h8, w8
+
+    cpu_inp = P.inp
+    del P
+
+    # ---- secondary workload: the main timed region only
+    secondary = None
+    if args.secondary != "none" and args.secondary != args.workload:
+        s = Problem(W.ALL_WORKLOADS[args.secondary], rank, args, dev, eas)
+        sms_, srecs, sclk = timed(s.step, args.steps, s.stream, trace=True)
+        assert eas.read_device_status(s.ws) == 0
+        _, stok = aggregate_ranks(0.0, float(s.Ta), dev)
+        srf, skern, sgemm, _ = breakdown(s, srecs, args.steps, sms_, sclk)
+        secondary = {s.w.name: {"value": stok / (sms_ / 1000.0), "unit": UNIT,
+                                "ms_per_step": sms_, "steps": args.steps,
+                                "config": {"T": s.T, "H": s.H, "V": s.V,
+                                           "active_tokens_per_rank": s.Ta},
+                                **rate_block(8.0 * s.Ta * s.H * s.V / (sms_ / 1000.0) / 1e12,
+                                             sclk),
+                                "roofline": srf, "kernels_ms_per_step": skern,
+                                "gemm_tflops": sgemm, "clocks": sclk}}
+        del s
 
     # ---- CPU oracle baseline (rank 0, N=1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n, t = oracle_sample_rate(inp, args.cpu_seconds)
+        n, t = oracle_sample_rate(cpu_inp, args.cpu_seconds)
         cpu = {"value": n / t, "unit": UNIT, "cores": host_cores(), "kind": "oracle",
                "sample": f"{n} random active rows at full H={H}, V={V}: fp64 forward + "
                          f"d-logits + dHidden + dW contribution, {t:.1f} s"}
 
     if rank == 0:
+        rb = rate_block(tflops, clocks)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -554,13 +670,18 @@ def main():
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "T": T, "H": H, "V": V,
                        "active_tokens_per_rank": Ta, "max_gap": args.max_gap,
-                       "rows": args.rows, "vocab_chunk": args.vocab_chunk or 16384,
+                       "rows": args.rows, "vocab_chunk": chunk,
+                       "workspace_bytes": eas.lmhead_workspace_size(T, H, V, torch.bfloat16,
+                                                                    args.vocab_chunk),
                        "parallelism": f"replicas x{world} (independent batches)",
                        "l2": "inputs larger than L2 (W alone is %.2f GB)" % (V * H * 2 / 1e9)},
             "tflops_active": tflops,
-            "frac_of_peak": tflops / pk["bf16_sustained"],
+            "frac_of_peak": rb["frac_of_peak"],
             "peak_tflops": pk["bf16_sustained"],
             "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+            "frac_of_burst": rb["frac_of_burst"], "peak_burst_tflops": pk["bf16"],
+            "frac_of_nominal": rb["frac_of_nominal"], "peak_nominal_tflops": NOMINAL_BF16_TFLOPS,
+            "frac_per_clock": rb["frac_per_clock"],
             "roofline": roofline,
             "kernels_ms_per_step": kernels,
             "gemm_tflops": gemm_tflops,
@@ -568,6 +689,7 @@ def main():
             "gpu_launches": launches,
             "dense_ablation": dense,
             "forward_only": fwd_only,
+            "secondary": secondary,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks,

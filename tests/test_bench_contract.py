@@ -42,10 +42,57 @@ def test_reference_arm_other_ranks_print_nothing():
                       "--warmup", "1"], env={"RANK": "1", "WORLD_SIZE": "2"}) == []
 
 
+def test_default_workload_is_the_largest_one_gpu_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    from entropy_active_span_gb300 import workloads as W
+    old = sys.argv
+    sys.argv = ["bench.py"]
+    try:
+        a = bench.parse_args()
+    finally:
+        sys.argv = old
+    largest = max((w for w in W.WORKLOADS.values() if w.dtype == "bf16"), key=lambda w: w.T * w.H)
+    assert a.workload == largest.name == "long_256k"
+    assert a.secondary == "rl_16k"
+
+
+def test_fractions_use_four_denominators():
+    sys.path.insert(0, ROOT)
+    import bench
+    pk = dict(bf16=2000.0, bf16_sustained=1600.0, hbm=7000.0, source="test")
+    f = bench.fractions(1000.0, pk, 1500.0, 152)
+    assert abs(f["frac_sustained"] - 1000 / 1600) < 1e-12
+    assert abs(f["frac_burst"] - 1000 / 2000) < 1e-12
+    assert abs(f["frac_nominal"] - 1000 / 2250) < 1e-12
+    assert abs(f["per_clock_peak_tflops"] - 152 * 8192 * 1500e6 / 1e12) < 1e-9
+    assert abs(f["frac_per_clock"] - 1000 / f["per_clock_peak_tflops"]) < 1e-12
+    assert bench.fractions(1000.0, pk, None, 152)["frac_per_clock"] is None
+    # e4m3: every denominator doubles
+    f2 = bench.fractions(1000.0, pk, 1500.0, 152, peak_scale=2.0)
+    assert abs(f2["frac_per_clock"] - f["frac_per_clock"] / 2) < 1e-12
+
+
+def test_traffic_is_keyed_by_kernel_build_and_launch_shape():
+    sys.path.insert(0, ROOT)
+    import bench
+    sha = bench.source_sha()
+    # a record exists only for the shapes that were captured, never reused for others
+    got, src = bench.recorded_traffic("bwd_chunk_gemm_tc", "no_such_workload/c16384")
+    assert got is None and src is None
+    for path in os.listdir(os.path.join(ROOT, "profiles")):
+        for line in open(os.path.join(ROOT, "profiles", path)):
+            parts = line.split()
+            if parts[:1] == ["traffic"]:
+                assert len(parts) == 5 and "/c" in parts[2] and int(parts[3]) > 0
+                if parts[4] == sha:
+                    assert bench.recorded_traffic(parts[1], parts[2])[0] == int(parts[3])
+
+
 @pytest.mark.gpu
 def test_own_arm_line():
     (d,) = run_bench(["--workload", "rl_4k_v32k", "--steps", "3", "--warmup", "3",
-                      "--no-dense", "--no-cpu-baseline"])
+                      "--no-dense", "--no-cpu-baseline", "--secondary", "none"])
     for k in BASE_KEYS + ("roofline", "clocks", "gpu_launches", "phases", "forward_only"):
         assert k in d, k
     assert d["n_gpus"] == 1 and d["scaling"] == "weak" and d["dtype"] == "bf16"
@@ -53,7 +100,12 @@ def test_own_arm_line():
     rf = d["roofline"]
     assert rf["bound"] == "tensor" and rf["unit"] == "TFLOP/s" and rf["peak"] > 0
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
-    assert "traffic" in rf
+    assert abs(rf["frac_burst"] - rf["achieved"] / rf["peak_burst"]) < 1e-9
+    assert abs(rf["frac_nominal"] - rf["achieved"] / 2250.0) < 1e-9
+    if d["clocks"]:
+        assert rf["frac_per_clock"] > 0 and rf["sm_mhz_median"] == d["clocks"]["sm_mhz"]
+    # no ncu capture was made at this shape: the traffic must be null
+    assert "traffic" in rf and rf["traffic"] is None
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     c = d["clocks"]
