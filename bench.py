@@ -273,6 +273,19 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def wait_first(self, limit_s: float = 5.0):
+        """Blocks until nvidia-smi has written its first sample (or limit_s)."""
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < limit_s:
+            if self.proc.poll() is not None:
+                return
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                return
+            time.sleep(0.02)
+
     def stop(self):
         if self.proc is None:
             return None
@@ -412,13 +425,17 @@ def main():
 
     def timed(fn, k, stream, trace=False, marks=None, clocks=True):
         """Warm-up, then k timed calls bracketed by barrier + synchronize;
-        returns (ms per call over the slowest rank, trace records, clocks)."""
+        returns (ms per call over the slowest rank, trace records, clocks).
+        The clock sampler runs from before the warm-up (also under load) to
+        the end of the timed calls, so that short regions still get samples."""
+        sampler = ClockSampler(uuid) if (clocks and rank == 0) else None
+        if sampler:
+            sampler.wait_first()
         for _ in range(args.warmup):
             fn()
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        sampler = ClockSampler(uuid) if (clocks and rank == 0) else None
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if trace:
             eas.trace_enable(True)

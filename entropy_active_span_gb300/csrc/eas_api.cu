@@ -213,7 +213,7 @@ struct Layout {
   int n_chunks;
   long long ldz;       // staging row pitch (elements)
   size_t status, sched, head_end;                // cleared at the start of each call
-  size_t row_map, pack_of, hp;                   // common part
+  size_t row_map, pack_of, tile_rows, hp;        // common part
   size_t pm, ps, pu, zt, fwd_counter;             // forward part
   size_t dz, dz2, acc, counters;                  // backward part (two staging buffers)
   size_t fwd_end, bwd_end, total;
@@ -237,6 +237,7 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   L.head_end = o;
   L.row_map = o; o = align_up(o + 4 * static_cast<size_t>(L.T_pad > 0 ? L.T_pad : 1));
   L.pack_of = o; o = align_up(o + 4 * static_cast<size_t>(T > 0 ? T : 1));
+  L.tile_rows = o; o = align_up(o + 8 * static_cast<size_t>(rowmap_tiles(T > 0 ? T : 1)));
   L.hp = o; o = align_up(o + esz * static_cast<size_t>(L.T_pad) * H);
   const size_t common = o;
   L.pm = o; o = align_up(o + 4 * static_cast<size_t>(L.n_vt) * L.T_pad);
@@ -295,7 +296,8 @@ eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* span
     EAS_CUDA(launch_rowmap(mask, spans, num_spans, cap, T, (flags & EAS_ROWS_SPAN) ? 1 : 0,
                            targets, static_cast<int>(t_lo),
                            static_cast<int>(t_hi < 0x7fffffffLL ? t_hi : 0x7fffffffLL),
-                           at<int>(ws, L.row_map), at<int>(ws, L.pack_of), at<Sched>(ws, L.sched),
+                           at<int>(ws, L.row_map), at<int>(ws, L.pack_of),
+                           at<long long>(ws, L.tile_rows), at<Sched>(ws, L.sched),
                            at<DevStatus>(ws, L.status), s),
              "rowmap");
   }
@@ -309,9 +311,16 @@ eas_status prologue(const void* hidden, const uint8_t* mask, const int32_t* span
   return EAS_OK;
 }
 
+#ifndef EAS_BAND_MB
+#define EAS_BAND_MB 48
+#endif
+#ifndef EAS_BAND_MIN
+#define EAS_BAND_MIN 1
+#endif
 int group_for(long long bytes_per_mtile, long long num_m) {
-  const long long budget = 48LL << 20;
+  const long long budget = static_cast<long long>(EAS_BAND_MB) << 20;
   long long g = bytes_per_mtile > 0 ? budget / bytes_per_mtile : num_m;
+  if (g < EAS_BAND_MIN) g = EAS_BAND_MIN;
   if (g < 1) g = 1;
   if (g > num_m) g = num_m;
   return static_cast<int>(g > 0 ? g : 1);

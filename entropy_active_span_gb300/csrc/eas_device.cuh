@@ -33,12 +33,15 @@ struct DevStatus {
 };
 
 // Row schedule produced on the device from the spans (R = packed rows,
-// R_pad = R rounded up to the 256-row tensor-core tile).
+// R_pad = R rounded up to the 256-row tensor-core tile).  `bad` and `ticket`
+// are the row-map kernels' own bookkeeping (zero at the start of each call).
 struct Sched {
   int R;
   int R_pad;
   int S;
-  int pad;
+  int bad;      // spans failed validation (set by any CTA of the count pass)
+  int ticket;   // CTAs of the count pass that have finished
+  int pad[3];
 };
 
 __device__ __forceinline__ void report(DevStatus* st, int code, int where, int info) {

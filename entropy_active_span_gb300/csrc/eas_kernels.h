@@ -13,10 +13,13 @@ struct Sched;
 // ---- span builder and row schedule (eas_sched.cu) ----
 cudaError_t launch_spans_build(const uint8_t* mask, long long T, int max_gap, int* spans,
                                long long cap, int* num_spans, DevStatus* st, cudaStream_t s);
+// Row schedule in two passes over tiles of 4096 tokens; tile_rows holds
+// rowmap_tiles(T) entries of scratch.
+long long rowmap_tiles(long long T);
 cudaError_t launch_rowmap(const uint8_t* mask, const int* spans, const int* num_spans,
                           long long cap, long long T, int span_rows, const int* targets, int t_lo,
-                          int t_hi, int* row_map, int* pack_of, Sched* sched, DevStatus* st,
-                          cudaStream_t s);
+                          int t_hi, int* row_map, int* pack_of, long long* tile_rows,
+                          Sched* sched, DevStatus* st, cudaStream_t s);
 cudaError_t launch_gather_rows(const void* src, void* dst, const int* row_map, const Sched* sched,
                                long long T_pad, long long row_bytes, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const float* pm, const float* ps, const float* pu, const float* zt,

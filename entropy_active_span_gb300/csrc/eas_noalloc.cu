@@ -8,6 +8,7 @@
 // only input and output buffers.  This entry point serves them with a fixed
 // scratch area compiled into the library: every GPU that loads the library
 // reserves it until the process exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -24,39 +25,94 @@ constexpr size_t kStaticScratchBytes = EAS_STATIC_SCRATCH_BYTES;
 // device symbol: its device address comes from cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
+// Device address of the scratch area in the context current on this thread.
+//
+// Module addresses belong to a context.  The primary context of a device, a
+// context the host created through the driver API and made current, and the
+// primary context re-created after cudaDeviceReset each hold their own copy of
+// the array at their own address.  The address is therefore looked up once per
+// context (for most callers: once per device, in its primary context), with
+// that context current, and cached under the context's unique ID, which the
+// driver never hands out twice in a process; a call made in a context not seen
+// before looks the address up again.  The lookup allocates nothing, but the
+// first one in a context loads the library's device code into that context,
+// so the first call in a context should come before any stream capture.
 
-// Device address of the scratch area on the current device, looked up once
-// per device (with that device current) and cached.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+struct CtxApi {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+const CtxApi& ctx_api() {
+  static CtxApi api;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      api.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      api.get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  return api;
+}
+
+// Unique ID of the context current on this thread; false if there is none.
+bool current_ctx_id(const CtxApi& api, unsigned long long* id) {
+  CUcontext ctx = nullptr;
+  if (api.get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return api.get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+constexpr int kCacheSlots = 64;
+struct CacheSlot {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+std::mutex g_mu;
+CacheSlot g_cache[kCacheSlots] = {};
+int g_cache_next = 0;
+
+eas_status lookup_error(cudaError_t e) {
+  char msg[256];
+  snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+  eas::set_last_error(msg);
+  return EAS_ERR_CUDA;
+}
+
 eas_status static_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    char msg[256];
-    snprintf(msg, sizeof(msg), "cudaGetDevice: %s", cudaGetErrorString(e));
-    eas::set_last_error(msg);
+  const CtxApi& api = ctx_api();
+  if (!api.get_current || !api.get_id) {
+    eas::set_last_error("cuCtxGetCurrent / cuCtxGetId unavailable from the driver");
     return EAS_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    eas::set_last_error("device ordinal out of range for the static scratch table");
-    return EAS_ERR_UNSUPPORTED;
-  }
+  unsigned long long id = 0;
+  bool have_ctx = current_ctx_id(api, &id);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      char msg[256];
-      snprintf(msg, sizeof(msg), "cudaGetSymbolAddress(static scratch): %s",
-               cudaGetErrorString(e));
-      eas::set_last_error(msg);
-      return EAS_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
+  if (have_ctx) {
+    for (const CacheSlot& c : g_cache)
+      if (c.ptr != nullptr && c.ctx_id == id) {
+        *out = c.ptr;
+        return EAS_OK;
+      }
   }
-  *out = g_scratch_ptr[dev];
+  // set-up in this context: with no context current yet, the lookup makes the
+  // current device's primary context current first
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || p == nullptr) return lookup_error(e);
+  if (!have_ctx) have_ctx = current_ctx_id(api, &id);
+  if (have_ctx) {
+    g_cache[g_cache_next] = CacheSlot{id, p};
+    g_cache_next = (g_cache_next + 1) % kCacheSlots;
+  }
+  *out = p;
   return EAS_OK;
 }
 

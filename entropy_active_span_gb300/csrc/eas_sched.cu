@@ -9,7 +9,9 @@
 //
 // Kernels:
 //   spans_build_kernel   mask -> spans[S][2], S                 (one CTA)
-//   rowmap_kernel        spans + mask -> validated row schedule (one CTA)
+//   rowmap_count_kernel, rowmap_write_kernel
+//                        spans + mask -> validated row schedule (one CTA per
+//                        4096 tokens, two passes)
 //   gather_rows_kernel   hidden rows of the schedule -> packed copy
 //   combine_kernel       per-vocab-tile softmax partials -> lse, entropy, logp
 //   zero_unpacked_rows_kernel  dhidden rows that no GEMM tile writes -> 0
@@ -161,99 +163,181 @@ spans_build_kernel(const uint8_t* __restrict__ mask, long long T, int max_gap,
 // reads kStInvalidSpans.  Active tokens whose target lies outside [t_lo, t_hi)
 // set kStInvalidArg (their outputs are then meaningless; nothing is read out
 // of bounds).
-__global__ void __launch_bounds__(kScanThreads)
-rowmap_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
-              const int* __restrict__ num_spans, long long cap, long long T, int span_rows,
-              const int* __restrict__ targets, int t_lo, int t_hi,
-              int* __restrict__ row_map, int* __restrict__ pack_of, Sched* sched,
-              DevStatus* st) {
-  __shared__ int sm_i[32];
-  __shared__ int bad;
-  const int S_raw = *num_spans;
-  if (threadIdx.x == 0) bad = 0;
-  __syncthreads();
-  int S = S_raw;
-  if (S_raw < 0 || static_cast<long long>(S_raw) > cap) {
-    if (threadIdx.x == 0) {
-      report(st, S_raw < 0 ? kStInvalidSpans : kStSpanCapacity, 2, S_raw);
-      bad = 1;
-    }
-    S = 0;
+//
+// Two passes over tiles of kRmTile tokens, one CTA per tile:
+//   rowmap_count_kernel  validates, counts each tile's listed rows into
+//                        tile_rows[tile]; the CTA that finishes last turns
+//                        the counts into exclusive offsets and writes R, R_pad;
+//   rowmap_write_kernel  writes row_map / pack_of of its tile from its offset.
+namespace {
+
+constexpr int kRmThreads = 256;
+constexpr int kRmItems = 16;
+constexpr int kRmTile = kRmThreads * kRmItems;   // 4096 tokens per CTA
+constexpr int kRmWarps = kRmThreads / 32;
+
+// Block-wide exclusive sum of one long long per thread (kRmThreads threads);
+// `total` receives the block's sum.
+__device__ __forceinline__ long long rm_excl_sum(long long v, long long* sm, long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  for (int k = threadIdx.x; k < S; k += kScanThreads) {
+  if (lane == 31) sm[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = (lane < kRmWarps) ? sm[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < kRmWarps) sm[lane] = w;
+  }
+  __syncthreads();
+  const long long before = warp ? sm[warp - 1] : 0;
+  total = sm[kRmWarps - 1];
+  __syncthreads();
+  return before + x - v;
+}
+
+// The listed rows among this thread's kRmItems tokens starting at t0: bit i
+// of the result is set when token t0 + i is listed.  `uncovered` is set when
+// an active token lies outside every span.
+__device__ __forceinline__ uint32_t rm_select(const uint8_t* __restrict__ mask,
+                                              const int* __restrict__ spans, int S, long long T,
+                                              long long t0, int span_rows, bool& uncovered) {
+  // largest k with start_k <= t0 (or -1)
+  int lo = 0, hi = S;  // search in [lo, hi)
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<long long>(spans[2 * mid]) <= t0) lo = mid + 1; else hi = mid;
+  }
+  int k = lo - 1;
+  uint32_t sel = 0;
+#pragma unroll 4
+  for (int i = 0; i < kRmItems; ++i) {
+    const long long t = t0 + i;
+    if (t >= T) break;
+    while (k + 1 < S && static_cast<long long>(spans[2 * (k + 1)]) <= t) ++k;
+    const bool covered = (k >= 0) && (t < static_cast<long long>(spans[2 * k + 1]));
+    const bool active = mask[t] != 0;
+    if (active && !covered) uncovered = true;
+    if (covered && (span_rows || active)) sel |= 1u << i;
+  }
+  return sel;
+}
+
+// Span count after the capacity check (0 when num_spans is out of range).
+__device__ __forceinline__ int rm_span_count(const int* num_spans, long long cap) {
+  const int S_raw = *num_spans;
+  return (S_raw < 0 || static_cast<long long>(S_raw) > cap) ? 0 : S_raw;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kRmThreads)
+rowmap_count_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
+                    const int* __restrict__ num_spans, long long cap, long long T, int span_rows,
+                    const int* __restrict__ targets, int t_lo, int t_hi,
+                    long long* __restrict__ tile_rows, Sched* sched, DevStatus* st) {
+  __shared__ long long sm_l[32];
+  __shared__ int last;
+  const int S_raw = *num_spans;
+  const int S = rm_span_count(num_spans, cap);
+  if (S != S_raw && blockIdx.x == 0 && threadIdx.x == 0) {
+    report(st, S_raw < 0 ? kStInvalidSpans : kStSpanCapacity, 2, S_raw);
+    atomicExch(&sched->bad, 1);
+  }
+  // span validity: sorted, non-empty, inside [0, T)
+  for (long long k = static_cast<long long>(blockIdx.x) * kRmThreads + threadIdx.x; k < S;
+       k += static_cast<long long>(gridDim.x) * kRmThreads) {
     const int s = spans[2 * k], e = spans[2 * k + 1];
     bool ok = (s >= 0) && (s < e) && (static_cast<long long>(e) <= T);
     if (k > 0) ok = ok && (spans[2 * k - 1] <= s);
-    if (!ok) bad = 1;
+    if (!ok) atomicExch(&sched->bad, 1);
   }
-  __syncthreads();
-  if (bad) S = 0;
-
-  long long R = 0;
-  const long long tile = static_cast<long long>(kScanThreads) * kScanItems;
-  for (long long base = 0; base < T; base += tile) {
-    const long long t0 = base + static_cast<long long>(threadIdx.x) * kScanItems;
-    // largest k with start_k <= t0 (or -1)
-    int lo = 0, hi = S;  // search in [lo, hi)
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (static_cast<long long>(spans[2 * mid]) <= t0) lo = mid + 1; else hi = mid;
-    }
-    int k = lo - 1;
-    uint32_t sel = 0;
-    int cnt = 0;
-    bool uncovered = false;
-#pragma unroll 4
-    for (int i = 0; i < kScanItems; ++i) {
+  const long long t0 = static_cast<long long>(blockIdx.x) * kRmTile +
+                       static_cast<long long>(threadIdx.x) * kRmItems;
+  bool uncovered = false;
+  const uint32_t sel = rm_select(mask, spans, S, T, t0, span_rows, uncovered);
+  if (targets != nullptr) {
+    for (int i = 0; i < kRmItems; ++i) {
       const long long t = t0 + i;
       if (t >= T) break;
-      while (k + 1 < S && static_cast<long long>(spans[2 * (k + 1)]) <= t) ++k;
-      const bool covered = (k >= 0) && (t < static_cast<long long>(spans[2 * k + 1]));
-      const bool active = mask[t] != 0;
-      if (active && !covered) uncovered = true;
-      if (active && targets != nullptr) {
+      if (mask[t] != 0) {
         const int tg = targets[t];
         if (tg < t_lo || tg >= t_hi) report(st, kStInvalidArg, 3, static_cast<int>(t));
       }
-      if (covered && (span_rows || active)) {
-        sel |= 1u << i;
-        ++cnt;
-      }
     }
-    if (uncovered) bad = 1;
-    int total;
-    const int excl = block_excl_sum(cnt, sm_i, total);
-    long long idx = R + excl;
-    for (int i = 0; i < kScanItems; ++i) {
-      const long long t = t0 + i;
-      if (t >= T) break;
-      if (sel & (1u << i)) {
-        row_map[idx] = static_cast<int>(t);
-        pack_of[t] = static_cast<int>(idx);
-        ++idx;
-      } else {
-        pack_of[t] = -1;
-      }
-    }
-    R += total;
+  }
+  if (uncovered) atomicExch(&sched->bad, 1);
+  __threadfence();     // this thread's flags before the CTA's ticket below
+  long long total;
+  rm_excl_sum(__popc(sel), sm_l, total);
+  if (threadIdx.x == 0) {
+    tile_rows[blockIdx.x] = total;
+    __threadfence();
+    last = (atomicAdd(&sched->ticket, 1) == static_cast<int>(gridDim.x) - 1);
   }
   __syncthreads();
-  if (bad) {
-    for (long long t = threadIdx.x; t < T; t += kScanThreads) pack_of[t] = -1;
-    if (threadIdx.x == 0) {
-      report(st, kStInvalidSpans, 2, -1);
-      sched->R = 0;
-      sched->R_pad = 0;
-      sched->S = S_raw;
-    }
+  if (!last) return;
+  // the last CTA: every count and every `bad` flag of the grid is visible
+  __threadfence();
+  const int n = gridDim.x;
+  long long carry = 0;
+  for (int base = 0; base < n; base += kRmThreads) {
+    const int i = base + threadIdx.x;
+    const long long v = (i < n) ? *reinterpret_cast<volatile long long*>(&tile_rows[i]) : 0;
+    long long part;
+    const long long ex = rm_excl_sum(v, sm_l, part);
+    if (i < n) tile_rows[i] = carry + ex;
+    carry += part;
+  }
+  if (threadIdx.x == 0) {
+    const bool bad = *reinterpret_cast<volatile int*>(&sched->bad) != 0;
+    if (bad) report(st, kStInvalidSpans, 2, -1);
+    sched->R = bad ? 0 : static_cast<int>(carry);
+    sched->R_pad = bad ? 0 : static_cast<int>((carry + 255) / 256 * 256);
+    sched->S = S_raw;
+  }
+}
+
+__global__ void __launch_bounds__(kRmThreads)
+rowmap_write_kernel(const uint8_t* __restrict__ mask, const int* __restrict__ spans,
+                    const int* __restrict__ num_spans, long long cap, long long T, int span_rows,
+                    const long long* __restrict__ tile_rows, int* __restrict__ row_map,
+                    int* __restrict__ pack_of, const Sched* __restrict__ sched) {
+  __shared__ long long sm_l[32];
+  const long long t0 = static_cast<long long>(blockIdx.x) * kRmTile +
+                       static_cast<long long>(threadIdx.x) * kRmItems;
+  if (sched->bad) {
+    for (int i = 0; i < kRmItems; ++i)
+      if (t0 + i < T) pack_of[t0 + i] = -1;
     return;
   }
-  const long long R_pad = (R + 255) / 256 * 256;
-  for (long long r = R + threadIdx.x; r < R_pad; r += kScanThreads) row_map[r] = -1;
-  if (threadIdx.x == 0) {
-    sched->R = static_cast<int>(R);
-    sched->R_pad = static_cast<int>(R_pad);
-    sched->S = S_raw;
+  const int S = rm_span_count(num_spans, cap);
+  bool uncovered = false;
+  const uint32_t sel = rm_select(mask, spans, S, T, t0, span_rows, uncovered);
+  long long total;
+  long long idx = tile_rows[blockIdx.x] + rm_excl_sum(__popc(sel), sm_l, total);
+  for (int i = 0; i < kRmItems; ++i) {
+    const long long t = t0 + i;
+    if (t >= T) break;
+    if (sel & (1u << i)) {
+      row_map[idx] = static_cast<int>(t);
+      pack_of[t] = static_cast<int>(idx);
+      ++idx;
+    } else {
+      pack_of[t] = -1;
+    }
+  }
+  if (blockIdx.x == gridDim.x - 1) {
+    const long long R = sched->R, R_pad = sched->R_pad;
+    for (long long r = R + threadIdx.x; r < R_pad; r += kRmThreads) row_map[r] = -1;
   }
 }
 
@@ -481,12 +565,21 @@ cudaError_t launch_spans_build(const uint8_t* mask, long long T, int max_gap, in
   return cudaGetLastError();
 }
 
+long long rowmap_tiles(long long T) { return (T + kRmTile - 1) / kRmTile; }
+
 cudaError_t launch_rowmap(const uint8_t* mask, const int* spans, const int* num_spans,
                           long long cap, long long T, int span_rows, const int* targets, int t_lo,
-                          int t_hi, int* row_map, int* pack_of, Sched* sched, DevStatus* st,
-                          cudaStream_t s) {
-  rowmap_kernel<<<1, kScanThreads, 0, s>>>(mask, spans, num_spans, cap, T, span_rows, targets,
-                                           t_lo, t_hi, row_map, pack_of, sched, st);
+                          int t_hi, int* row_map, int* pack_of, long long* tile_rows,
+                          Sched* sched, DevStatus* st, cudaStream_t s) {
+  const long long n = rowmap_tiles(T);
+  if (n <= 0) return cudaSuccess;
+  if (n > 0x7fffffffLL) return cudaErrorInvalidValue;
+  rowmap_count_kernel<<<static_cast<unsigned>(n), kRmThreads, 0, s>>>(
+      mask, spans, num_spans, cap, T, span_rows, targets, t_lo, t_hi, tile_rows, sched, st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  rowmap_write_kernel<<<static_cast<unsigned>(n), kRmThreads, 0, s>>>(
+      mask, spans, num_spans, cap, T, span_rows, tile_rows, row_map, pack_of, sched);
   return cudaGetLastError();
 }
 

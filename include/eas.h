@@ -294,9 +294,13 @@ eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
  *     EAS_ERR_WORKSPACE before anything is launched, and eas_last_error()
  *     gives the bytes needed (eas_lmhead_fwd with a workspace has no limit).
  *     For bf16 the need is about T * (2H + 12 ceil(V/256) + 16) bytes.
- *   - The first call on a device looks up the array's device address on that
- *     device (cudaGetSymbolAddress, with that device current); make that first
- *     call before any stream capture.
+ *   - Set-up: the first call in a context looks up the array's device
+ *     address there (cudaGetSymbolAddress, with that context current) and
+ *     caches it under the context's unique ID.  For most callers that is the
+ *     first call on each device, in its primary context; it happens again in
+ *     a context the host created and made current through the driver API, and
+ *     after cudaDeviceReset (each context holds its own copy of the array).
+ *     Make the first call in a context before any stream capture.
  *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call
  *     (leave eas_trace_enable off, since tracing creates CUDA events).
  *   - All calls share the one array, and it keeps what the last call left
@@ -304,8 +308,12 @@ eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
  *     overlap on the GPU (different streams, or different host threads
  *     without ordering) race on the array and give wrong results: order them.
  *   - The device status word lives in the shared array and cannot be read
- *     back through this entry point; as with eas_lmhead_fwd, spans that fail
- *     validation leave every output zero.
+ *     back through this entry point, so errors only the device can see go
+ *     unreported here: spans that fail validation leave every output zero
+ *     (as with eas_lmhead_fwd), and an active row whose target lies outside
+ *     [0, V) gets meaningless outputs with no error.  Callers that cannot
+ *     vouch for their spans and targets should use eas_lmhead_fwd and
+ *     eas_read_device_status.
  */
 #define EAS_STATIC_SCRATCH_BYTES (64ull << 20)
 
@@ -321,7 +329,8 @@ eas_status eas_lmhead_fwd_noalloc(const void* hidden, const void* weight,
 /*
  * Waits for `stream`, then returns the status word the device wrote into
  * workspace `ws` during the last call that used it (EAS_OK if none).  This is
- * the only entry point that synchronises the host.
+ * the only entry point that synchronises the host (cudaStreamSynchronize on
+ * `stream`); every other call only enqueues work.
  */
 eas_status eas_read_device_status(const void* ws, void* stream);
 
