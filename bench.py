@@ -120,11 +120,12 @@ def fractions(tflops: float, pk: dict, sm_mhz, sms: int, peak_scale: float = 1.0
 
 
 def source_sha() -> str:
-    """sha256[:16] of the tensor-core kernel sources (identifies a capture's kernel)."""
+    """sha256[:16] of the tensor-core kernel sources and of the host code that
+    sets their launch shapes and rasters (identifies a capture's build)."""
     import hashlib
     csrc = os.path.join(ROOT, "entropy_active_span_gb300", "csrc")
     src = "".join(open(os.path.join(csrc, f)).read()
-                  for f in ("eas_gemm_tc.cu", "eas_device.cuh", "eas_kernels.h"))
+                  for f in ("eas_gemm_tc.cu", "eas_device.cuh", "eas_kernels.h", "eas_api.cu"))
     return hashlib.sha256(src.encode()).hexdigest()[:16]
 
 
@@ -294,32 +295,36 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm, mx, reasons, mem, pw, temp = [], None, set(), [], [], []
+        rows = []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
-                pw.append(float(parts[2]))
+                r = {"sm": float(parts[0]), "max": float(parts[1]), "pw": float(parts[2]),
+                     "why": {n for n, v in zip(names, parts[4:8]) if v.lower() == "active"}}
                 if len(parts) >= 10:
-                    mem.append(float(parts[8]))
-                    temp.append(float(parts[9]))
+                    r["mem"], r["temp"] = float(parts[8]), float(parts[9])
             except ValueError:
                 continue
-            for name, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(name)
+            rows.append(r)
         os.unlink(self.path)
-        if not sm:
+        if not rows:
             return None
-        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-               "samples": len(sm), "power_w_median": statistics.median(pw) if pw else None}
+        # samples under load: power above 60 % of the highest draw seen (the
+        # sampler starts before the warm-up, so its first sample can be idle)
+        top = max(r["pw"] for r in rows)
+        loaded = [r for r in rows if r["pw"] >= 0.6 * top] or rows
+        reasons = set().union(*(r["why"] for r in loaded))
+        out = {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+               "sm_max_mhz": rows[-1]["max"], "reasons": sorted(reasons),
+               "samples": len(rows), "samples_under_load": len(loaded),
+               "power_w_median": statistics.median(r["pw"] for r in loaded)}
+        mem = [r["mem"] for r in loaded if "mem" in r]
         if mem:
             out["mem_mhz"] = statistics.median(mem)
-            out["temp_c_max"] = max(temp)
+            out["temp_c_max"] = max(r["temp"] for r in rows if "temp" in r)
         return out
 
 

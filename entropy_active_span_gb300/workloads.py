@@ -76,6 +76,11 @@ PROFILE_WORKLOADS = {
         "rl_16k_v32k", 16384, 4096, 32768, "bf16", 1002, "rl_prompts_1024",
         description="rl_16k's rows and mask with V=32768: its backward launches have the "
                     "shapes of rl_16k's (about 2 GB on the device)"),
+    "long_16k_v48k": Workload(
+        "long_16k_v48k", 16384, 8192, 49152, "bf16", 1105, "rl_prompts_8192",
+        description="long_256k's H, mask structure and vocabulary chunk on 2 sequences x 8192 "
+                    "and V=49152 (3 chunks): tiles with long_256k's K extents, about 5 GB "
+                    "on the device"),
 }
 ALL_WORKLOADS = {**WORKLOADS, **PROFILE_WORKLOADS}
 

@@ -114,3 +114,29 @@ def test_own_arm_line():
     assert d["gpu_launches"] > 0
     p = d["phases"]
     assert abs(p["spans_ms"] + p["fwd_ms"] + p["bwd_ms"] - d["ms_per_step"]) < 0.1 * d["ms_per_step"]
+
+
+def test_clock_median_counts_samples_under_load_only(tmp_path):
+    """The sampler starts before the warm-up, so its first sample can be
+    idle; the median clock and power come from samples under load."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    class Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            pass
+
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.path = str(tmp_path / "clocks.csv")
+    idle = "1995, 2070, 180.0, 0x0, Not Active, Not Active, Not Active, Not Active, 3996, 40"
+    busy = ("{mhz}, 2070, {w}, 0x4, Not Active, Not Active, Not Active, Active, 3996, 55")
+    open(c.path, "w").write("\n".join([idle, busy.format(mhz=1400, w=1360.0),
+                                       busy.format(mhz=1380, w=1370.0),
+                                       busy.format(mhz=1390, w=1365.0)]) + "\n")
+    c.proc = Done()
+    out = c.stop()
+    assert out["sm_mhz"] == 1390 and out["samples"] == 4 and out["samples_under_load"] == 3
+    assert out["reasons"] == ["sw_power_cap"] and out["power_w_median"] == 1365.0
