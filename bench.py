@@ -26,6 +26,7 @@ NumPy) on a bounded sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -254,7 +255,7 @@ def reference_arm(args, rank):
 # -------------------------------------------------------------- clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
               "clocks.mem,temperature.gpu")
@@ -262,6 +263,7 @@ class ClockSampler:
     def __init__(self, uuid: str | None):
         self.proc = None
         self.path = None
+        self.window = None      # (start, end) of the timed region, local wall clock
         try:
             fd, self.path = tempfile.mkstemp(suffix=".csv")
             os.close(fd)
@@ -299,10 +301,15 @@ class ClockSampler:
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                r = {"sm": float(parts[0]), "max": float(parts[1]), "pw": float(parts[2]),
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                ts = None
+            parts = parts[1:]
+            try:
+                r = {"ts": ts, "sm": float(parts[0]), "max": float(parts[1]), "pw": float(parts[2]),
                      "why": {n for n, v in zip(names, parts[4:8]) if v.lower() == "active"}}
                 if len(parts) >= 10:
                     r["mem"], r["temp"] = float(parts[8]), float(parts[9])
@@ -312,14 +319,22 @@ class ClockSampler:
         os.unlink(self.path)
         if not rows:
             return None
-        # samples under load: power above 60 % of the highest draw seen (the
-        # sampler starts before the warm-up, so its first sample can be idle)
-        top = max(r["pw"] for r in rows)
-        loaded = [r for r in rows if r["pw"] >= 0.6 * top] or rows
+        # samples of the timed region (when there are enough of them), else
+        # every sample under load: power above 60 % of the highest draw seen
+        # (the sampler starts before the warm-up; its first sample can be idle)
+        sel, basis = rows, "all samples"
+        if self.window is not None:
+            w0, w1 = self.window
+            inside = [r for r in rows if r["ts"] is not None and w0 <= r["ts"] <= w1]
+            if len(inside) >= 3:
+                sel, basis = inside, "timed region"
+        top = max(r["pw"] for r in sel)
+        loaded = [r for r in sel if r["pw"] >= 0.6 * top] or sel
         reasons = set().union(*(r["why"] for r in loaded))
         out = {"sm_mhz": statistics.median(r["sm"] for r in loaded),
                "sm_max_mhz": rows[-1]["max"], "reasons": sorted(reasons),
-               "samples": len(rows), "samples_under_load": len(loaded),
+               "samples": len(rows), "samples_used": len(loaded),
+               "basis": basis + ", under load",
                "power_w_median": statistics.median(r["pw"] for r in loaded)}
         mem = [r["mem"] for r in loaded if "mem" in r]
         if mem:
@@ -444,6 +459,7 @@ def main():
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if trace:
             eas.trace_enable(True)
+        t_start = datetime.datetime.now()
         e0.record(stream)
         for i in range(k):
             if marks is None:
@@ -452,6 +468,8 @@ def main():
                 fn(marks=marks[i])
         e1.record(stream)
         torch.cuda.synchronize()
+        if sampler:
+            sampler.window = (t_start, datetime.datetime.now())
         clk = sampler.stop() if sampler else None
         recs = None
         if trace:

@@ -196,6 +196,30 @@ eas_status make_map_bf16(CUtensorMap* m, const void* base, long long cols, long 
   return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, ld, box_rows);
 }
 
+// MN-major operand [rows = k][cols = m or n] as a 3-D map {64 columns, rows,
+// 64-column blocks}: one box {64, 64 k-rows, 2 blocks} lands in shared memory
+// as two 8 KB blocks [block][k-row][64 columns], the layout of two 2-D boxes.
+// Columns past `cols` in the last block are read from the row's padding
+// (within ld); blocks and rows past the end read as zero.
+eas_status make_map_bf16_mn3(CUtensorMap* m, const void* base, long long cols, long long rows,
+                             long long ld) {
+  EncodeTiledFn enc;
+  eas_status s = get_encoder(&enc);
+  if (s != EAS_OK) return s;
+  if (ld < (cols + 63) / 64 * 64) return fail(EAS_ERR_INVALID_ARG, "row pitch below block width");
+  cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>((cols + 63) / 64)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(EAS_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d) for [%lld x %lld] ld %lld",
+                static_cast<int>(r), rows, cols, ld);
+  return EAS_OK;
+}
+
 eas_status make_map_u8(CUtensorMap* m, const void* base, long long cols, long long rows,
                        long long ld, int box_rows) {
   return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, cols, rows, ld, box_rows);
@@ -636,8 +660,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
     if ((st = make_map_bf16(&hp_k, at<char>(ws, L.hp), H, L.T_pad, H, 128)) != EAS_OK) return st;
     if ((st = make_map_bf16(&w_k, weight, H, V, H, tc_tile_rows() == 256 ? 128 : 256)) != EAS_OK)
       return st;
-    if ((st = make_map_bf16(&w_mn, weight, H, V, H, 64)) != EAS_OK) return st;
-    if ((st = make_map_bf16(&hp_mn, at<char>(ws, L.hp), H, L.T_pad, H, 64)) != EAS_OK) return st;
+    if ((st = make_map_bf16_mn3(&w_mn, weight, H, V, H)) != EAS_OK) return st;
+    if ((st = make_map_bf16_mn3(&hp_mn, at<char>(ws, L.hp), H, L.T_pad, H)) != EAS_OK) return st;
     TcArgs base;
     memset(&base, 0, sizeof(base));
     base.sched = sched;
@@ -672,7 +696,7 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
         void* dz = staging[p % 2];
         CUtensorMap dz_k, dz_mn;
         if ((st = make_map_bf16(&dz_k, dz, live, L.T_pad, L.ldz, 128)) != EAS_OK) return st;
-        if ((st = make_map_bf16(&dz_mn, dz, live, L.T_pad, L.ldz, 64)) != EAS_OK) return st;
+        if ((st = make_map_bf16_mn3(&dz_mn, dz, live, L.T_pad, L.ldz)) != EAS_OK) return st;
         TcJob& w = a.jobs[a.n_jobs++];
         w.tmA = dz_mn;
         w.tmB = hp_mn;

@@ -23,7 +23,10 @@
 // Tiles are 256 x 256 and computed by a cluster of two CTAs (the two SMs of a
 // TPC) with tcgen05.mma.cta_group::2: CTA r loads A rows [128r, 128r+128) and
 // B columns [128r, 128r+128) of the tile (seven 32 KB stages of K = 64; the e4m3
-// forward uses three 64 KB stages of two k-blocks),
+// forward uses three 64 KB stages of two k-blocks).  A K-major operand comes in
+// one 2-D TMA box per k-block, an MN-major one (dHidden's B, dW's A and B) in
+// one 3-D box {64 columns, 64 k-rows, 2 column blocks}, so the producer issues
+// two TMA instructions per k-block whatever the kind;
 // and each CTA's TMEM receives its 128 x 256 half of the accumulator.  CTA
 // layout (192 threads): warp 0 = TMA producer (lane 0; on the even CTA it also
 // fetches tile indices and publishes them to both CTAs), warp 1 = MMA issuer
@@ -490,6 +493,16 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// 3-D TMA load: coordinates (c0, c1, c2) of the map's three dimensions.
+__device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // e4m3 k-block: 128 one-byte elements per 128-byte swizzle row.
 constexpr int kKbFp8 = 128;
 
@@ -692,16 +705,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
             }
           } else if (kind == kTcDHidden) {
             tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(dB + j * 8192, &jb.tmB, bar, ncol + j * 64, jb.v0 + k0);
+            tma_load_3d_pair(dB, &jb.tmB, bar, 0, jb.v0 + k0, ncol >> 6);
           } else {
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(dA + j * 8192, &jb.tmA, bar, mrow + j * 64, k0);
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-              tma_load_2d_pair(dB + j * 8192, &jb.tmB, bar, ncol + j * 64, k0);
+            tma_load_3d_pair(dA, &jb.tmA, bar, 0, k0, mrow >> 6);
+            tma_load_3d_pair(dB, &jb.tmB, bar, 0, k0, ncol >> 6);
           }
           if (++stage == kPStages) {
             stage = 0;

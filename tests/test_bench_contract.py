@@ -118,8 +118,10 @@ def test_own_arm_line():
 
 def test_clock_median_counts_samples_under_load_only(tmp_path):
     """The sampler starts before the warm-up, so its first sample can be
-    idle; the median clock and power come from samples under load."""
+    idle; the median clock and power come from samples under load, and from
+    the timed region alone when it holds enough samples."""
     sys.path.insert(0, ROOT)
+    import datetime
     import bench
 
     class Done:
@@ -129,14 +131,27 @@ def test_clock_median_counts_samples_under_load_only(tmp_path):
         def wait(self, timeout=None):
             pass
 
-    c = bench.ClockSampler.__new__(bench.ClockSampler)
-    c.path = str(tmp_path / "clocks.csv")
-    idle = "1995, 2070, 180.0, 0x0, Not Active, Not Active, Not Active, Not Active, 3996, 40"
-    busy = ("{mhz}, 2070, {w}, 0x4, Not Active, Not Active, Not Active, Active, 3996, 55")
-    open(c.path, "w").write("\n".join([idle, busy.format(mhz=1400, w=1360.0),
-                                       busy.format(mhz=1380, w=1370.0),
-                                       busy.format(mhz=1390, w=1365.0)]) + "\n")
-    c.proc = Done()
-    out = c.stop()
-    assert out["sm_mhz"] == 1390 and out["samples"] == 4 and out["samples_under_load"] == 3
-    assert out["reasons"] == ["sw_power_cap"] and out["power_w_median"] == 1365.0
+    def run(lines, window=None):
+        c = bench.ClockSampler.__new__(bench.ClockSampler)
+        c.path = str(tmp_path / "clocks.csv")
+        open(c.path, "w").write("\n".join(lines) + "\n")
+        c.proc = Done()
+        c.window = window
+        return c.stop()
+
+    t0 = datetime.datetime(2026, 1, 1, 12, 0, 0)
+
+    def line(sec, mhz, w, cap="Active"):
+        ts = (t0 + datetime.timedelta(seconds=sec)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (f"{ts}, {mhz}, 2070, {w}, 0x4, Not Active, Not Active, Not Active, {cap}, "
+                "3996, 55")
+
+    lines = [line(0.0, 1995, 180.0, "Not Active"), line(0.2, 1500, 1360.0),
+             line(0.4, 1400, 1365.0), line(0.6, 1380, 1370.0), line(0.8, 1390, 1366.0)]
+    out = run(lines)
+    assert out["sm_mhz"] == 1395 and out["samples"] == 5 and out["samples_used"] == 4
+    assert out["reasons"] == ["sw_power_cap"] and out["power_w_median"] == 1365.5
+    # the timed region holds the last three samples: the warm-up's 1500 MHz drops out
+    win = (t0 + datetime.timedelta(seconds=0.3), t0 + datetime.timedelta(seconds=0.9))
+    out = run(lines, win)
+    assert out["sm_mhz"] == 1390 and out["samples_used"] == 3 and out["basis"].startswith("timed")
