@@ -719,6 +719,10 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
         h.v0 = static_cast<int>(v0);
         h.vc_live = static_cast<int>(live);
         h.first_chunk = (p == 0);
+        if (p != L.n_chunks - 1 &&
+            (st = make_map_2d(&h.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, at<float>(ws, L.acc), H,
+                              L.T_pad, H, 32)) != EAS_OK)
+          return st;
         h.last_chunk = (p == L.n_chunks - 1);
         tiles += num_m_max * cdiv(H, kTcBN);
         trace_kind = kTrDProjGemm;
@@ -736,7 +740,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
         d.group_m = group_for(tc_tile_rows() * H * 2LL, num_m_max);
         d.v0 = static_cast<int>(v0);
         d.vc_live = static_cast<int>(live);
-        d.dz = staging[c % 2];
+        if ((st = make_map_bf16(&d.tmD, staging[c % 2], L.ldz, L.T_pad, L.ldz, 32)) != EAS_OK)
+          return st;
         tiles += num_m_max * cdiv(live, kTcBN);
         if (c > 0) trace_kind = kTrBwdChunkGemm;
       }

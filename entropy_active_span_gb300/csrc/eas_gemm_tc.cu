@@ -22,12 +22,14 @@
 //
 // Tiles are 256 x 256 and computed by a cluster of two CTAs (the two SMs of a
 // TPC) with tcgen05.mma.cta_group::2: CTA r loads A rows [128r, 128r+128) and
-// B columns [128r, 128r+128) of the tile (seven 32 KB stages of K = 64; the e4m3
-// forward uses three 64 KB stages of two k-blocks).  A K-major operand comes in
-// one 2-D TMA box per k-block, an MN-major one (dHidden's B, dW's A and B) in
-// one 3-D box {64 columns, 64 k-rows, 2 column blocks}, so the producer issues
-// two TMA instructions per k-block whatever the kind;
-// and each CTA's TMEM receives its 128 x 256 half of the accumulator.  CTA
+// B columns [128r, 128r+128) of the tile (32 KB stages of K = 64: seven in the
+// forward, six in the backward, whose epilogues stage their output in the
+// remaining 32 KB and write it with TMA; the e4m3 forward uses three 64 KB
+// stages of two k-blocks).  A K-major operand comes in one 2-D TMA box per
+// k-block, an MN-major one (dHidden's B, dW's A and B) in one 3-D box
+// {64 columns, 64 k-rows, 2 column blocks}, so the producer issues two TMA
+// instructions per k-block whatever the kind.  Each CTA's TMEM receives its
+// 128 x 256 half of the accumulator.  CTA
 // layout (192 threads): warp 0 = TMA producer (lane 0; on the even CTA it also
 // fetches tile indices and publishes them to both CTAs), warp 1 = MMA issuer
 // (lane 0 of the even CTA) and TMEM owner, warps 2..5 = epilogue, one
@@ -198,6 +200,38 @@ struct RowScalars {
   bool active;
 };
 
+// TMA store of a shared-memory box to the map's coordinates (c0, c1), as one
+// bulk async-group of the issuing thread.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* smem_src,
+                                                  int c0, int c1) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // Coalesced row stores.  tcgen05.ld (32x32b) hands each lane one row of the
 // tile, so a lane storing its own row would touch 32 rows (32 memory lines)
 // per warp store.  octet_transpose regroups a chunk across each group of 8
@@ -276,33 +310,80 @@ __device__ __forceinline__ void dlogits_chunk(const TcJob& jb, uint32_t taddr, b
 }
 
 // d-logits tile rows into the bf16 staging buffer, 64 columns (128 bytes of a
-// row) per round.
-__device__ __forceinline__ void epi_dlogits(const TcArgs& a, const TcJob& jb, uint32_t tbase,
-                                            bool k_empty, long long r0, int n_blk, int row,
-                                            const RowScalars& rs) {
+// row) per round: the warp's 32 rows go to a 4 KB shared-memory box in the
+// 128-byte swizzled layout (16-byte chunk j of row l at chunk j ^ (l & 7)),
+// and lane 0 writes the box with a TMA store.  Two boxes per warp alternate;
+// `cnt` counts the warp's boxes so far.
+__device__ __forceinline__ void epi_dlogits(const TcJob& jb, uint32_t tbase, bool k_empty,
+                                            long long r0, int n_blk, int row,
+                                            const RowScalars& rs, uint8_t* sEpi, uint32_t& cnt) {
   const int n0 = n_blk * kTcBN;
   const int lane = row & 31;
-  const int i = lane & 7;
-  const long long r_oct = r0 + (row & ~31) + (lane & ~7);   // first row of this octet
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(jb.dz) + r_oct * a.ldz + n0;
+  const int q = row >> 5;
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 64; ++c) {
     uint32_t pk[32];
     dlogits_chunk(jb, tbase + c * 64, k_empty, n0 + c * 64, rs, pk);
     dlogits_chunk(jb, tbase + c * 64 + 32, k_empty, n0 + c * 64 + 32, rs, pk + 16);
-    octet_transpose(pk, i);
+    uint8_t* box = sEpi + ((cnt & 1u) * 4 + q) * 4096;
+    if (lane == 0) bulk_wait_read<1>();     // the box's previous store has read it
+    __syncwarp();
+    uint8_t* rowp = box + lane * 128;
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      uint4* o = reinterpret_cast<uint4*>(out + p * a.ldz + c * 64) + i;
-      *o = make_uint4(pk[4 * p], pk[4 * p + 1], pk[4 * p + 2], pk[4 * p + 3]);
-    }
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+          make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) tma_store_2d(&jb.tmD, box, n0 + c * 64, static_cast<int>(r0) + q * 32);
+    ++cnt;
   }
 }
 
-// dHidden: accumulate this chunk's product into the fp32 accumulator; the
-// last chunk converts to bf16 and scatters the row to its token (zeros for
-// gap rows whose mask byte is 0).
-__device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, uint32_t tbase,
+// dHidden of a chunk before the last: the warp's 32 rows x 32 columns of fp32
+// go to a 4 KB shared-memory box (128-byte swizzled) and lane 0 adds the box
+// into the fp32 accumulator [T_pad][H] with a TMA reduce-add (a TMA store on
+// the first chunk), so the L2 does the read-modify-write.  Each accumulator
+// element receives one add per launch, in chunk order across launches, so
+// the sum is deterministic.
+__device__ __forceinline__ void epi_dhidden_acc(const TcArgs& a, const TcJob& jb, uint32_t tbase,
+                                                bool k_empty, long long r0, int n_blk, int row,
+                                                uint8_t* sEpi, uint32_t& cnt) {
+  const int n0 = n_blk * kTcBN;
+  const int lane = row & 31;
+  const int q = row >> 5;
+#pragma unroll 1
+  for (int c = 0; c < kTcBN / 32; ++c) {
+    if (n0 + c * 32 >= a.H) break;
+    float v[32];
+    if (k_empty) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    } else {
+      tmem_ld32(tbase + c * 32, v);
+    }
+    uint8_t* box = sEpi + ((cnt & 1u) * 4 + q) * 4096;
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    uint8_t* rowp = box + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (jb.first_chunk) tma_store_2d(&jb.tmD, box, n0 + c * 32, static_cast<int>(r0) + q * 32);
+      else tma_reduce_add_2d(&jb.tmD, box, n0 + c * 32, static_cast<int>(r0) + q * 32);
+    }
+    ++cnt;
+  }
+}
+
+// dHidden of the last chunk (or the only one): this chunk's product plus the
+// accumulator (unless it is also the first chunk), converted to bf16 and
+// scattered to the rows' tokens (zeros for gap rows whose mask byte is 0).
+__device__ __forceinline__ void epi_dhidden_last(const TcArgs& a, const TcJob& jb, uint32_t tbase,
                                             bool k_empty, long long r0, int n_blk, int row, int tok,
                                             bool active) {
   const int n0 = n_blk * kTcBN;
@@ -314,12 +395,10 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, ui
   // (lane & ~7) + p)
   int tok_p[8];
   uint32_t act_bits = 0;
-  if (jb.last_chunk) {
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
-      tok_p[p] = __shfl_sync(0xffffffffu, tok, (lane & ~7) + p);
-      if (__shfl_sync(0xffffffffu, active ? 1 : 0, (lane & ~7) + p)) act_bits |= 1u << p;
-    }
+  for (int p = 0; p < 8; ++p) {
+    tok_p[p] = __shfl_sync(0xffffffffu, tok, (lane & ~7) + p);
+    if (__shfl_sync(0xffffffffu, active ? 1 : 0, (lane & ~7) + p)) act_bits |= 1u << p;
   }
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 32; ++c) {
@@ -342,22 +421,15 @@ __device__ __forceinline__ void epi_dhidden(const TcArgs& a, const TcJob& jb, ui
         v[4 * p + 3] += x.w;
       }
     }
-    if (!jb.last_chunk) {
 #pragma unroll
-      for (int p = 0; p < 8; ++p)
-        reinterpret_cast<float4*>(acc + p * a.H + c * 32)[i] =
-            make_float4(v[4 * p], v[4 * p + 1], v[4 * p + 2], v[4 * p + 3]);
-    } else {
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        if (tok_p[p] < 0) continue;
-        const bool on = (act_bits >> p) & 1u;
-        __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.dhidden) +
-                           static_cast<long long>(tok_p[p]) * a.H + n0 + c * 32;
-        reinterpret_cast<uint2*>(o)[i] =
-            make_uint2(on ? pack_bf16x2(v[4 * p], v[4 * p + 1]) : 0u,
-                       on ? pack_bf16x2(v[4 * p + 2], v[4 * p + 3]) : 0u);
-      }
+    for (int p = 0; p < 8; ++p) {
+      if (tok_p[p] < 0) continue;
+      const bool on = (act_bits >> p) & 1u;
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(a.dhidden) +
+                         static_cast<long long>(tok_p[p]) * a.H + n0 + c * 32;
+      reinterpret_cast<uint2*>(o)[i] =
+          make_uint2(on ? pack_bf16x2(v[4 * p], v[4 * p + 1]) : 0u,
+                     on ? pack_bf16x2(v[4 * p + 2], v[4 * p + 3]) : 0u);
     }
   }
 }
@@ -412,18 +484,21 @@ constexpr int kPM = 256;                          // rows of a pair tile
 constexpr int kPKBlockBytes = kPHalf * 128;       // one 128-byte-swizzled k-block: 16 KB
 
 // Pipeline stage geometry of an instantiation.  A stage holds kSub k-blocks
-// of each operand.  The bf16 kinds use seven stages of one k-block (32 KB
-// per CTA).  The e4m3 forward, whose MMAs finish a k-block in half the time,
-// uses three stages of two k-blocks (64 KB): half as many stage boundaries
-// per unit of work, 2 % faster there, while bf16 measured no better with them.
+// of each operand.  The bf16 forward uses seven stages of one k-block (32 KB
+// per CTA); the backward six, leaving 32 KB for the epilogues' TMA staging
+// (two 4 KB boxes per epilogue warp).  The e4m3 forward, whose MMAs finish a
+// k-block in half the time, uses three stages of two k-blocks (64 KB): half
+// as many stage boundaries per unit of work, 2 % faster there, while bf16
+// measured no better with them.
 template <int kMode>
 struct PipeGeo {
   static constexpr int kSub = (kMode == 2) ? 2 : 1;
-  static constexpr int kStages = (kMode == 2) ? 3 : 7;
+  static constexpr int kStages = (kMode == 2) ? 3 : (kMode == 1) ? 6 : 7;
   static constexpr int kABytes = kSub * kPKBlockBytes;
   static constexpr int kBBytes = kSub * kPKBlockBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 + 512;
+  static constexpr int kEpiBytes = (kMode == 1) ? 32768 : 0;
+  static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024 + 512;
 };
 // the backward's MN-major operands come in TMA boxes of one k-block's 64
 // k-rows (the host builds those tensor maps)
@@ -566,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kPStages * kPABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kPStages * kPBBytes);
+  uint8_t* sEpi = sB + kPStages * kPBBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sEpi + G::kEpiBytes);
   uint64_t* empty = full + kPStages;
   uint64_t* tfull = empty + kPStages;
   uint64_t* tempty = tfull + 2;
@@ -804,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
     // ------------------------------------------------ epilogue warps (both CTAs)
     const int q = warp & 3;
     const int row = q * 32 + lane;
+    uint32_t epi_cnt = 0;
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
       if (!mbar_wait_cl(&rfull[slot], (it / kRing) & 1, abort_flag, a.budget)) {
@@ -863,8 +940,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       } else if constexpr (kFwd) {
         epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
       } else {
-        if (kind == kTcDLogits) epi_dlogits(a, jb, tbase, k_empty, r0, w.tc.n, row, rs);
-        else if (kind == kTcDHidden) epi_dhidden(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
+        if (kind == kTcDLogits) epi_dlogits(jb, tbase, k_empty, r0, w.tc.n, row, rs, sEpi, epi_cnt);
+        else if (kind == kTcDHidden) {
+          if (jb.last_chunk) epi_dhidden_last(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
+          else epi_dhidden_acc(a, jb, tbase, k_empty, r0, w.tc.n, row, sEpi, epi_cnt);
+        }
         else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
       }
       tc_fence_before();
@@ -874,6 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         else mbar_arrive_cluster(tempty_leader0 + 8 * buf);
       }
     }
+    if (!kFwd && lane == 0) bulk_wait_all();   // every staged d-logits box written
   }
 
   tc_fence_before();

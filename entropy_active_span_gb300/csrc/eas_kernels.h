@@ -65,6 +65,8 @@ enum TcKind : int {
 struct TcJob {
   CUtensorMap tmA;   // A operand (see TcKind for the layout of each kind)
   CUtensorMap tmB;   // B operand
+  CUtensorMap tmD;   // TMA store target: the d-logits staging (dlogits), the fp32
+                     // accumulator (dhidden before the last chunk)
   int kind;
   int M_fixed;       // > 0: rows of the problem; 0: R_pad from sched
   int N;             // columns of the problem
@@ -74,7 +76,6 @@ struct TcJob {
   int vc_live;       // live columns of this chunk (dlogits / dweight)
   int first_chunk;   // dhidden: first chunk (store, do not accumulate)
   int last_chunk;    // dhidden: last chunk (convert and scatter to dhidden)
-  void* dz;          // dlogits: bf16 staging written by this job [T_pad][ldz]
 };
 
 constexpr int kMaxTcJobs = 3;
