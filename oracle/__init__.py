@@ -11,7 +11,8 @@ Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 """
 from .spans import active_spans, span_rows
 from .cp import cp_local_mask, cp_local_to_global
-from .fp8 import (dequantize_rows_e4m3, e4m3_decode, e4m3_encode_rne,
+from .fp8 import (dequantize_rows_e4m3, dequantized_rows, e4m3_decode, e4m3_encode_rne,
+                  lmhead_backward_e4m3, lmhead_backward_e4m3_rows_weighted,
                   quantize_rows_e4m3)
 from .lmhead import (lmhead_forward, lmhead_forward_rows, lmhead_dlogits_rows,
                      lmhead_backward, lmhead_backward_rows_weighted, loss_value)
@@ -20,5 +21,6 @@ __all__ = [
     "active_spans", "span_rows", "cp_local_mask", "cp_local_to_global", "lmhead_forward", "lmhead_forward_rows",
     "lmhead_dlogits_rows", "lmhead_backward", "lmhead_backward_rows_weighted",
     "loss_value", "e4m3_decode", "e4m3_encode_rne", "quantize_rows_e4m3",
-    "dequantize_rows_e4m3",
+    "dequantize_rows_e4m3", "dequantized_rows", "lmhead_backward_e4m3",
+    "lmhead_backward_e4m3_rows_weighted",
 ]

@@ -62,3 +62,55 @@ def quantize_rows_e4m3(x):
 def dequantize_rows_e4m3(codes, scales) -> np.ndarray:
     """float64 value of each quantised element: decode(q) * scale of its row."""
     return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[:, None]
+
+
+# ----------------------------------------------------------------------------
+# Backward of the e4m3 forward
+#
+# The pages give no FP8 backward; this is the reading the e4m3 training path
+# implements.  The d-logits are those of the logits the e4m3 forward computes
+# (z' = hq Wq^T with the row-dequantised operands hq, Wq), so they agree with
+# the lse and entropy that forward returned; they are then projected with the
+# unquantised operands, as the bf16 backward does:
+#   dZ' = g_lp (onehot(t) - p') - g_H p' (z' - lse' + H'),  p' = softmax(z'),
+#   dHidden = dZ' W,   dW = dZ'^T hidden.
+# Rows with mask 0 contribute nothing.
+# ----------------------------------------------------------------------------
+
+def dequantized_rows(x) -> np.ndarray:
+    """float64 values the e4m3 path computes with for a [R, H] operand:
+    per-row quantised (quantize_rows_e4m3) and dequantised."""
+    return dequantize_rows_e4m3(*quantize_rows_e4m3(np.asarray(x, dtype=np.float32)))
+
+
+def lmhead_backward_e4m3_rows_weighted(hidden_rows, W, Wq, t_rows, g_lp_rows, g_h_rows,
+                                       block: int = 256):
+    """dHidden rows and the dW contribution of a row subset under the reading
+    above; Wq = dequantized_rows(W) is passed in so that large W is quantised
+    once.  hidden_rows and W are the unquantised values."""
+    from .lmhead import lmhead_dlogits_rows
+    h = np.asarray(hidden_rows, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    hq = dequantized_rows(h)
+    dh = np.zeros_like(h)
+    dW = np.zeros_like(W)
+    n = h.shape[0]
+    for b in range(0, n, block):
+        sl = slice(b, min(n, b + block))
+        dz = lmhead_dlogits_rows(hq[sl], Wq, np.asarray(t_rows)[sl],
+                                 np.asarray(g_lp_rows)[sl], np.asarray(g_h_rows)[sl])
+        dh[sl] = dz @ W
+        dW += dz.T @ h[sl]
+    return dh, dW
+
+
+def lmhead_backward_e4m3(hidden, W, targets, mask, g_lp, g_h):
+    """dHidden [T, H] and dW [V, H] of the e4m3 path (reading above)."""
+    hidden = np.asarray(hidden, dtype=np.float64)
+    act = np.flatnonzero(np.asarray(mask).reshape(-1) != 0)
+    dhidden = np.zeros_like(hidden)
+    Wq = dequantized_rows(W)
+    dh, dW = lmhead_backward_e4m3_rows_weighted(hidden[act], W, Wq, np.asarray(targets)[act],
+                                                np.asarray(g_lp)[act], np.asarray(g_h)[act])
+    dhidden[act] = dh
+    return dhidden, dW
