@@ -89,6 +89,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-dense", action="store_true")
     p.add_argument("--no-forward-only", action="store_true")
+    p.add_argument("--no-e4m3-training", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle sample (cpu_baseline)")
@@ -672,6 +673,47 @@ def main():
                                          "ratio 4.5/2.25)")
         del ws_fwd, ws8, h8, w8
 
+    # ---- training on e4m3 logits: hidden and W quantised every step (W
+    # changes every optimizer step), the e4m3 forward, and the e4m3 backward
+    # (d-logits recomputed from the e4m3 operands, dHidden and dW in bf16).
+    # Two of the four GEMMs run at the e4m3 rate, so the peak for its active
+    # FLOPs is 4/3 of every bf16 peak: 8u / (2u/P + 2u/(2P)).
+    e4m3_train = None
+    if not args.no_e4m3_training and H % 128 == 0:
+        h8 = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        hsc = torch.empty(T, dtype=torch.float32, device=dev)
+        w8 = torch.empty((V, H), dtype=torch.uint8, device=dev)
+        wsc = torch.empty(V, dtype=torch.float32, device=dev)
+        ws8 = eas.workspace(eas.lmhead_workspace_size(T, H, V, torch.uint8), dev)
+        wsb = eas.workspace(eas.lmhead_bwd_fp8_workspace_size(T, H, V, args.vocab_chunk), dev)
+
+        def train_e4m3():
+            eas.quantize_rows_e4m3(P.hidden, out=h8, scale=hsc)
+            eas.quantize_rows_e4m3(P.weight, out=w8, scale=wsc)
+            eas.build_active_spans(P.mask, args.max_gap, spans=P.spans, num_spans=P.ns,
+                                   ws=P.sws)
+            eas.lmhead_fwd_fp8(h8, hsc, w8, wsc, P.targets, P.mask, P.spans, P.ns, P.flags,
+                               ws=ws8, out=(P.lp, P.ent, P.lse))
+            eas.lmhead_bwd_fp8(P.glp, P.gh, P.hidden, P.weight, h8, hsc, w8, wsc, P.targets,
+                               P.mask, P.spans, P.ns, P.lse, P.ent, P.flags, args.vocab_chunk,
+                               ws=wsb, dhidden=P.dh, dweight=P.dw)
+
+        tms, trecs, tclk = timed(train_e4m3, abl_steps, P.stream, trace=True)
+        assert eas.read_device_status(wsb) == 0
+        tby = {}
+        for name, t in trecs:
+            tby[name] = tby.get(name, 0.0) + t / abl_steps
+        tf = 8.0 * Ta * H * V / (tms / 1000.0) / 1e12
+        e4m3_train = {"ms_per_step": tms, "steps": abl_steps,
+                      "active_tokens_per_s": tokens_all / (tms / 1000.0),
+                      **rate_block(tf, tclk, 4.0 / 3.0),
+                      "speedup_vs_bf16_step": ms / tms,
+                      "kernels_ms_per_step": {k: round(v, 3) for k, v in sorted(tby.items())},
+                      "peak_kind": "every bf16 denominator x 4/3 (forward and recompute at the "
+                                   "nominal e4m3 rate, 2x bf16; dHidden and dW in bf16)",
+                      "note": "includes quantising hidden and W every step"}
+        del ws8, wsb, h8, w8
+
     cpu_inp = P.inp
     del P
 
@@ -729,6 +771,7 @@ def main():
             "gpu_launches": launches,
             "dense_ablation": dense,
             "forward_only": fwd_only,
+            "e4m3_training": e4m3_train,
             "secondary": secondary,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -25,7 +25,7 @@ __all__ = [
     "FusedLMHeadLogprob",
     "fused_logprob_entropy", "trace_enable", "trace_read", "lmhead_fwd_shard",
     "lmhead_combine_shards", "lmhead_bwd_shard", "cp_local_layout", "quantize_rows_e4m3",
-    "lmhead_fwd_fp8",
+    "lmhead_fwd_fp8", "lmhead_bwd_fp8", "lmhead_bwd_fp8_workspace_size",
 ]
 
 
@@ -239,6 +239,47 @@ def lmhead_fwd_fp8(hidden_e4m3, hidden_scale, weight_e4m3, weight_scale, targets
         _ptr(spans), _ptr(num_spans), int(spans.shape[0]), T, H, V, int(flags), _ptr(lp),
         _ptr(ent), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)))
     return lp, ent, lse
+
+
+def lmhead_bwd_fp8_workspace_size(T: int, H: int, V: int, vocab_chunk: int = 0) -> int:
+    return int(_lib.load().eas_lmhead_bwd_fp8_workspace_size(T, H, V, vocab_chunk))
+
+
+def lmhead_bwd_fp8(g_logprob, g_entropy, hidden, weight, hidden_e4m3, hidden_scale, weight_e4m3,
+                   weight_scale, targets, mask, spans, num_spans, lse, entropy,
+                   flags: int = EAS_ROWS_ACTIVE, vocab_chunk: int = 0, ws=None, dhidden=None,
+                   dweight=None):
+    """Backward of the e4m3 forward: d-logits of the e4m3 logits, projected
+    with the bf16 operands.  Returns (dHidden bf16, dW fp32)."""
+    dev = hidden.device
+    T, H = hidden.shape
+    V = weight.shape[0]
+    h8, w8 = _as_codes(hidden_e4m3), _as_codes(weight_e4m3)
+    for t, n, d in ((g_logprob, "g_logprob", torch.float32), (g_entropy, "g_entropy", torch.float32),
+                    (lse, "lse", torch.float32), (entropy, "entropy", torch.float32),
+                    (hidden, "hidden", torch.bfloat16), (weight, "weight", torch.bfloat16),
+                    (h8, "hidden_e4m3", torch.uint8), (w8, "weight_e4m3", torch.uint8),
+                    (hidden_scale, "hidden_scale", torch.float32),
+                    (weight_scale, "weight_scale", torch.float32),
+                    (targets, "targets", torch.int32), (mask, "mask", torch.uint8),
+                    (spans, "spans", torch.int32), (num_spans, "num_spans", torch.int32)):
+        _need(t, n, d, dev)
+    if h8.shape != (T, H) or w8.shape != (V, H):
+        raise ValueError("the e4m3 operands must have the shapes of hidden and weight")
+    if dhidden is None:
+        dhidden = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if dweight is None:
+        dweight = torch.empty((V, H), dtype=torch.float32, device=dev)
+    _need(dhidden, "dhidden", torch.bfloat16, dev)
+    _need(dweight, "dweight", torch.float32, dev)
+    if ws is None:
+        ws = workspace(lmhead_bwd_fp8_workspace_size(T, H, V, vocab_chunk), dev)
+    _lib.check(_lib.load().eas_lmhead_bwd_fp8(
+        _ptr(g_logprob), _ptr(g_entropy), _ptr(hidden), _ptr(weight), _ptr(h8), _ptr(hidden_scale),
+        _ptr(w8), _ptr(weight_scale), _ptr(targets), _ptr(mask), _ptr(spans), _ptr(num_spans),
+        int(spans.shape[0]), _ptr(lse), _ptr(entropy), T, H, V, int(flags), int(vocab_chunk),
+        _ptr(dhidden), _ptr(dweight), _ptr(ws), ws.numel(), _stream(dev)))
+    return dhidden, dweight
 
 
 def lmhead_fwd_shard(hidden, weight_shard, v_lo: int, targets, mask, spans, num_spans,

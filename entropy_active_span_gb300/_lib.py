@@ -43,6 +43,10 @@ SIGNATURES = {
     "eas_quantize_rows_e4m3": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _P, _P, _P]),
     "eas_lmhead_fwd_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                           _U32, _P, _P, _P, _P, _SZ, _P]),
+    "eas_lmhead_bwd_fp8_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
+    "eas_lmhead_bwd_fp8": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64,
+                                          _P, _P, _I64, _I64, _I64, _U32, _I64, _P, _P, _P, _SZ,
+                                          _P]),
     "eas_lmhead_fwd_shard": (ctypes.c_int, [_P, _P, _I64, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
                                             ctypes.c_int, _U32, _P, _P, _SZ, _P]),
     "eas_lmhead_combine_shards": (ctypes.c_int, [_P, _I32, _I64, _P, _P, _P, _P, _P]),

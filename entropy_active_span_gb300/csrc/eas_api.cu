@@ -94,19 +94,20 @@ long long wait_budget() {
 // launches.  Backward tensor-core launches are named by their jobs:
 // dlogits_gemm_tc (d-logits of chunk 0), bwd_chunk_gemm_tc (dW and dHidden of
 // chunk c-1 with the d-logits of chunk c), dproj_gemm_tc (dW and dHidden of
-// the last chunk).
+// the last chunk); the e4m3 backward runs dlogits_gemm_tc_e4m3 (d-logits of a
+// chunk) and dproj_gemm_tc (dW and dHidden of that chunk) per chunk.
 
 enum TraceKind : int {
   kTrSpans = 0, kTrRowmap, kTrGather, kTrFwdGemm, kTrCombine, kTrZeroRows,
   kTrDLogitsGemm, kTrDProjGemm, kTrUnused, kTrSimtFwd, kTrSimtDLogits,
-  kTrSimtDHidden, kTrSimtDWeight, kTrMemset, kTrBwdChunkGemm, kTrCount
+  kTrSimtDHidden, kTrSimtDWeight, kTrMemset, kTrBwdChunkGemm, kTrDLogitsFp8Gemm, kTrCount
 };
 
 const char* const kTraceNames[kTrCount] = {
     "spans_build", "rowmap", "gather_rows", "fwd_gemm_tc", "combine", "zero_rows",
     "dlogits_gemm_tc", "dproj_gemm_tc", "unused", "fwd_gemm_simt",
     "dlogits_gemm_simt", "dhidden_gemm_simt", "dweight_gemm_simt", "memset",
-    "bwd_chunk_gemm_tc"};
+    "bwd_chunk_gemm_tc", "dlogits_gemm_tc_e4m3"};
 
 struct TraceRec {
   int kind;
@@ -276,11 +277,27 @@ Layout layout(long long T, long long H, long long V, eas_dtype dt, long long chu
   if (dt == EAS_BF16 && L.n_chunks > 1) o = align_up(o + esz * static_cast<size_t>(L.T_pad) * L.ldz);
   L.acc = o;
   if (L.n_chunks > 1) o = align_up(o + 4 * static_cast<size_t>(L.T_pad) * H);
-  L.counters = o; o = align_up(o + sizeof(int) * static_cast<size_t>(L.n_chunks + 1));
+  L.counters = o; o = align_up(o + sizeof(int) * static_cast<size_t>(2 * L.n_chunks + 1));
   L.bwd_end = o;
   L.total = L.fwd_end > L.bwd_end ? L.fwd_end : L.bwd_end;
   return L;
 }
+
+// The e4m3 backward's packed e4m3 rows [T_pad][H] (one byte each), placed
+// after the bf16 layout, which holds its bf16 packed rows, staging and
+// accumulator.
+size_t fp8_rows_offset(const Layout& L) { return align_up(L.total); }
+size_t fp8_bwd_total(const Layout& L, long long H) {
+  return fp8_rows_offset(L) + align_up(static_cast<size_t>(L.T_pad) * static_cast<size_t>(H));
+}
+
+// e4m3 operands of the e4m3 backward's recompute.
+struct Fp8Operands {
+  const uint8_t* hidden;   // [T, H] codes
+  const float* hscale;     // [T]
+  const uint8_t* weight;   // [V, H] codes
+  const float* wscale;     // [V]
+};
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -597,12 +614,25 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
                            const int32_t* spans, const int32_t* num_spans, int64_t cap,
                            const float* lse, const float* entropy, int64_t T, int64_t H, int64_t V,
                            eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
-                           float* dweight, int64_t t_off, bool sharded, void* ws,
-                           size_t ws_bytes, void* stream) {
+                           float* dweight, int64_t t_off, bool sharded, const Fp8Operands* f8,
+                           void* ws, size_t ws_bytes, void* stream) {
   eas_status st = check_shape(T, H, V, dtype);
   if (st != EAS_OK) return st;
   if (dtype == EAS_E4M3)
-    return fail(EAS_ERR_UNSUPPORTED, "the backward takes bf16 or fp32 operands");
+    return fail(EAS_ERR_UNSUPPORTED,
+                "the backward takes bf16 or fp32 operands (e4m3: eas_lmhead_bwd_fp8)");
+  if (f8) {
+    if (dtype != EAS_BF16) return fail(EAS_ERR_INVALID_ARG, "the e4m3 backward projects in bf16");
+    if (H % 128 != 0)
+      return fail(EAS_ERR_UNSUPPORTED, "e4m3 path needs H %% 128 == 0 (H=%lld)", (long long)H);
+    if (flags & EAS_REUSE_FWD_ROWS)
+      return fail(EAS_ERR_INVALID_ARG,
+                  "the e4m3 backward packs its own rows (EAS_REUSE_FWD_ROWS not accepted)");
+    if (T > 0 && (!f8->hidden || !f8->hscale)) return fail(EAS_ERR_INVALID_ARG, "null pointer");
+    if (!f8->weight || !f8->wscale) return fail(EAS_ERR_INVALID_ARG, "null pointer");
+    if (!aligned(f8->hidden, 16) || !aligned(f8->weight, 16))
+      return fail(EAS_ERR_INVALID_ARG, "e4m3 operands must be 16-byte aligned");
+  }
   const bool reuse = (flags & EAS_REUSE_FWD_ROWS) != 0;
   flags &= ~EAS_REUSE_FWD_ROWS;
   if (flags > 1u) return fail(EAS_ERR_INVALID_ARG, "unknown flags %u", flags);
@@ -616,7 +646,8 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
       !aligned(dweight, 16) || !aligned(ws, 256))
     return fail(EAS_ERR_INVALID_ARG, "tensors must be 16-byte and ws 256-byte aligned");
   const Layout L = layout(T, H, V, dtype, vocab_chunk);
-  if (ws_bytes < L.bwd_end) return fail(EAS_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, L.bwd_end);
+  const size_t need = f8 ? fp8_bwd_total(L, H) : L.bwd_end;
+  if (ws_bytes < need) return fail(EAS_ERR_WORKSPACE, "workspace %zu < %zu", ws_bytes, need);
   DevInfo di;
   st = device_info(&di);
   if (st != EAS_OK) return st;
@@ -627,12 +658,19 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
                   sharded ? 0x7fffffffLL : static_cast<long long>(V), ws, L, di, s);
     if (st != EAS_OK) return st;
   }
+  if (f8 && T > 0) {
+    Trace tr_(kTrGather, s);
+    EAS_CUDA(launch_gather_rows(f8->hidden, at<char>(ws, fp8_rows_offset(L)),
+                                at<int>(ws, L.row_map), at<Sched>(ws, L.sched), L.T_pad, H,
+                                di.sms, s),
+             "gather e4m3 rows");
+  }
   // (with reuse, the row schedule and packed rows of the preceding forward
   // stay where that call's layout put them: the shared part of the layout
   // does not depend on vocab_chunk; the status word is kept)
   {
     Trace tr_(kTrMemset, s);
-    EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.counters), 0, sizeof(int) * (L.n_chunks + 1), s),
+    EAS_CUDA(cudaMemsetAsync(at<char>(ws, L.counters), 0, sizeof(int) * (2 * L.n_chunks + 1), s),
              "clear counters");
   }
   if (T == 0) {
@@ -652,10 +690,6 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
   const long long num_m_max = L.T_pad / tc_tile_rows();
 
   if (dtype == EAS_BF16) {
-    // Launch c (0..n) runs dW and dHidden of chunk c-1 (reading staging
-    // buffer (c-1)%2) next to the d-logits of chunk c (writing buffer c%2):
-    // the jobs of one launch are independent and share the machine, and each
-    // launch boundary orders a chunk's d-logits before its projections.
     CUtensorMap hp_k, w_k, w_mn, hp_mn;
     if ((st = make_map_bf16(&hp_k, at<char>(ws, L.hp), H, L.T_pad, H, 128)) != EAS_OK) return st;
     if ((st = make_map_bf16(&w_k, weight, H, V, H, tc_tile_rows() == 256 ? 128 : 256)) != EAS_OK)
@@ -682,72 +716,115 @@ static eas_status bwd_impl(const float* g_logprob, const float* g_entropy, const
     base.dhidden = dhidden;
     base.dW = dweight;
     void* staging[2] = {at<char>(ws, L.dz), at<char>(ws, L.n_chunks > 1 ? L.dz2 : L.dz)};
-    for (int c = 0; c <= L.n_chunks; ++c) {
-      TcArgs a = base;
-      a.tile_counter = at<int>(ws, L.counters) + c;
-      long long tiles = 0;
-      int trace_kind = kTrDLogitsGemm;
-      // projections of the previous chunk: dW (longest tiles when R is
-      // large) and dHidden first, the short d-logits tiles last
-      if (c > 0) {
-        const int p = c - 1;
-        const long long v0 = p * L.vc;
-        const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
-        void* dz = staging[p % 2];
-        CUtensorMap dz_k, dz_mn;
-        if ((st = make_map_bf16(&dz_k, dz, live, L.T_pad, L.ldz, 128)) != EAS_OK) return st;
-        if ((st = make_map_bf16_mn3(&dz_mn, dz, live, L.T_pad, L.ldz)) != EAS_OK) return st;
-        TcJob& w = a.jobs[a.n_jobs++];
-        w.tmA = dz_mn;
-        w.tmB = hp_mn;
-        w.kind = kTcDWeight;
-        w.M_fixed = static_cast<int>(live);
-        w.N = static_cast<int>(H);
-        w.K_fixed = 0;
-        w.group_m = group_for(tc_tile_rows() * L.T_pad * 2LL, cdiv(live, tc_tile_rows()));
-        w.v0 = static_cast<int>(v0);
-        w.vc_live = static_cast<int>(live);
-        tiles += cdiv(live, tc_tile_rows()) * cdiv(H, kTcBN);
-        TcJob& h = a.jobs[a.n_jobs++];
-        h.tmA = dz_k;
-        h.tmB = w_mn;
-        h.kind = kTcDHidden;
-        h.M_fixed = 0;
-        h.N = static_cast<int>(H);
-        h.K_fixed = static_cast<int>(live);
-        h.group_m = group_for(tc_tile_rows() * live * 2LL, num_m_max);
-        h.v0 = static_cast<int>(v0);
-        h.vc_live = static_cast<int>(live);
-        h.first_chunk = (p == 0);
-        if (p != L.n_chunks - 1 &&
-            (st = make_map_2d(&h.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, at<float>(ws, L.acc), H,
-                              L.T_pad, H, 32)) != EAS_OK)
-          return st;
-        h.last_chunk = (p == L.n_chunks - 1);
-        tiles += num_m_max * cdiv(H, kTcBN);
-        trace_kind = kTrDProjGemm;
-      }
-      if (c < L.n_chunks) {
-        const long long v0 = c * L.vc;
-        const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
-        TcJob& d = a.jobs[a.n_jobs++];
-        d.tmA = hp_k;
-        d.tmB = w_k;
-        d.kind = kTcDLogits;
-        d.M_fixed = 0;
-        d.N = static_cast<int>(live);
-        d.K_fixed = static_cast<int>(H);
-        d.group_m = group_for(tc_tile_rows() * H * 2LL, num_m_max);
-        d.v0 = static_cast<int>(v0);
-        d.vc_live = static_cast<int>(live);
-        if ((st = make_map_bf16(&d.tmD, staging[c % 2], L.ldz, L.T_pad, L.ldz, 32)) != EAS_OK)
-          return st;
-        tiles += num_m_max * cdiv(live, kTcBN);
-        if (c > 0) trace_kind = kTrBwdChunkGemm;
-      }
-      {
+    // dW and dHidden of chunk p, reading staging buffer p%2
+    auto add_projections = [&](TcArgs& a, int p, long long& tiles) -> eas_status {
+      const long long v0 = p * L.vc;
+      const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
+      void* dz = staging[p % 2];
+      CUtensorMap dz_k, dz_mn;
+      eas_status e;
+      if ((e = make_map_bf16(&dz_k, dz, live, L.T_pad, L.ldz, 128)) != EAS_OK) return e;
+      if ((e = make_map_bf16_mn3(&dz_mn, dz, live, L.T_pad, L.ldz)) != EAS_OK) return e;
+      TcJob& w = a.jobs[a.n_jobs++];
+      w.tmA = dz_mn;
+      w.tmB = hp_mn;
+      w.kind = kTcDWeight;
+      w.M_fixed = static_cast<int>(live);
+      w.N = static_cast<int>(H);
+      w.K_fixed = 0;
+      w.group_m = group_for(tc_tile_rows() * L.T_pad * 2LL, cdiv(live, tc_tile_rows()));
+      w.v0 = static_cast<int>(v0);
+      w.vc_live = static_cast<int>(live);
+      tiles += cdiv(live, tc_tile_rows()) * cdiv(H, kTcBN);
+      TcJob& h = a.jobs[a.n_jobs++];
+      h.tmA = dz_k;
+      h.tmB = w_mn;
+      h.kind = kTcDHidden;
+      h.M_fixed = 0;
+      h.N = static_cast<int>(H);
+      h.K_fixed = static_cast<int>(live);
+      h.group_m = group_for(tc_tile_rows() * live * 2LL, num_m_max);
+      h.v0 = static_cast<int>(v0);
+      h.vc_live = static_cast<int>(live);
+      h.first_chunk = (p == 0);
+      if (p != L.n_chunks - 1 &&
+          (e = make_map_2d(&h.tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, at<float>(ws, L.acc), H,
+                           L.T_pad, H, 32)) != EAS_OK)
+        return e;
+      h.last_chunk = (p == L.n_chunks - 1);
+      tiles += num_m_max * cdiv(H, kTcBN);
+      return EAS_OK;
+    };
+    // d-logits of chunk c into staging buffer c%2, from bf16 or e4m3 operands
+    auto add_dlogits = [&](TcArgs& a, int c, long long& tiles, bool e4m3,
+                           const CUtensorMap& tmA, const CUtensorMap& tmB) -> eas_status {
+      const long long v0 = c * L.vc;
+      const long long live = (V - v0) < L.vc ? (V - v0) : L.vc;
+      TcJob& d = a.jobs[a.n_jobs++];
+      d.tmA = tmA;
+      d.tmB = tmB;
+      d.kind = e4m3 ? kTcDLogitsFp8 : kTcDLogits;
+      d.M_fixed = 0;
+      d.N = static_cast<int>(live);
+      d.K_fixed = static_cast<int>(H);
+      d.group_m = group_for(tc_tile_rows() * H * (e4m3 ? 1LL : 2LL), num_m_max);
+      d.v0 = static_cast<int>(v0);
+      d.vc_live = static_cast<int>(live);
+      eas_status e = make_map_bf16(&d.tmD, staging[c % 2], L.ldz, L.T_pad, L.ldz, 32);
+      if (e != EAS_OK) return e;
+      tiles += num_m_max * cdiv(live, kTcBN);
+      return EAS_OK;
+    };
+    if (!f8) {
+      // Launch c (0..n) runs dW and dHidden of chunk c-1 (reading staging
+      // buffer (c-1)%2) next to the d-logits of chunk c (writing buffer c%2):
+      // the jobs of one launch are independent and share the machine, and
+      // each launch boundary orders a chunk's d-logits before its projections.
+      for (int c = 0; c <= L.n_chunks; ++c) {
+        TcArgs a = base;
+        a.tile_counter = at<int>(ws, L.counters) + c;
+        long long tiles = 0;
+        int trace_kind = kTrDLogitsGemm;
+        // projections of the previous chunk: dW (longest tiles when R is
+        // large) and dHidden first, the short d-logits tiles last
+        if (c > 0) {
+          if ((st = add_projections(a, c - 1, tiles)) != EAS_OK) return st;
+          trace_kind = kTrDProjGemm;
+        }
+        if (c < L.n_chunks) {
+          if ((st = add_dlogits(a, c, tiles, false, hp_k, w_k)) != EAS_OK) return st;
+          if (c > 0) trace_kind = kTrBwdChunkGemm;
+        }
         Trace tr_(trace_kind, s);
         EAS_CUDA(launch_tc_gemm(a, grid_for(tiles, di.sms), s), "backward gemm");
+      }
+    } else {
+      // e4m3 recompute: the d-logits GEMM runs in its own instantiation, so
+      // each chunk is two launches, the e4m3 d-logits, then dW and dHidden
+      CUtensorMap hp8_k, w8_k;
+      if ((st = make_map_u8(&hp8_k, at<char>(ws, fp8_rows_offset(L)), H, L.T_pad, H, 128)) !=
+          EAS_OK)
+        return st;
+      if ((st = make_map_u8(&w8_k, f8->weight, H, V, H, 128)) != EAS_OK) return st;
+      for (int c = 0; c < L.n_chunks; ++c) {
+        {
+          TcArgs a = base;
+          a.tile_counter = at<int>(ws, L.counters) + 2 * c;
+          a.hscale = f8->hscale;
+          a.wscale = f8->wscale;
+          long long tiles = 0;
+          if ((st = add_dlogits(a, c, tiles, true, hp8_k, w8_k)) != EAS_OK) return st;
+          Trace tr_(kTrDLogitsFp8Gemm, s);
+          EAS_CUDA(launch_tc_gemm(a, grid_for(tiles, di.sms), s), "backward gemm (e4m3)");
+        }
+        {
+          TcArgs a = base;
+          a.tile_counter = at<int>(ws, L.counters) + 2 * c + 1;
+          long long tiles = 0;
+          if ((st = add_projections(a, c, tiles)) != EAS_OK) return st;
+          Trace tr_(kTrDProjGemm, s);
+          EAS_CUDA(launch_tc_gemm(a, grid_for(tiles, di.sms), s), "backward gemm");
+        }
       }
     }
   } else {
@@ -831,8 +908,28 @@ eas_status eas_lmhead_bwd(const float* g_logprob, const float* g_entropy, const 
                           eas_dtype dtype, uint32_t flags, int64_t vocab_chunk, void* dhidden,
                           float* dweight, void* ws, size_t ws_bytes, void* stream) {
   return bwd_impl(g_logprob, g_entropy, hidden, weight, targets, mask, spans, num_spans, cap, lse,
-                  entropy, T, H, V, dtype, flags, vocab_chunk, dhidden, dweight, 0, false, ws,
-                  ws_bytes, stream);
+                  entropy, T, H, V, dtype, flags, vocab_chunk, dhidden, dweight, 0, false, nullptr,
+                  ws, ws_bytes, stream);
+}
+
+size_t eas_lmhead_bwd_fp8_workspace_size(int64_t T, int64_t H, int64_t V, int64_t vocab_chunk) {
+  if (T < 0 || H < 1 || V < 1) return 0;
+  return fp8_bwd_total(layout(T, H, V, EAS_BF16, vocab_chunk), H);
+}
+
+eas_status eas_lmhead_bwd_fp8(const float* g_logprob, const float* g_entropy, const void* hidden,
+                              const void* weight, const uint8_t* hidden_e4m3,
+                              const float* hidden_scale, const uint8_t* weight_e4m3,
+                              const float* weight_scale, const int32_t* targets,
+                              const uint8_t* mask, const int32_t* spans, const int32_t* num_spans,
+                              int64_t cap, const float* lse, const float* entropy, int64_t T,
+                              int64_t H, int64_t V, uint32_t flags, int64_t vocab_chunk,
+                              void* dhidden, float* dweight, void* ws, size_t ws_bytes,
+                              void* stream) {
+  const Fp8Operands f8{hidden_e4m3, hidden_scale, weight_e4m3, weight_scale};
+  return bwd_impl(g_logprob, g_entropy, hidden, weight, targets, mask, spans, num_spans, cap, lse,
+                  entropy, T, H, V, EAS_BF16, flags, vocab_chunk, dhidden, dweight, 0, false, &f8,
+                  ws, ws_bytes, stream);
 }
 
 eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
@@ -846,7 +943,7 @@ eas_status eas_lmhead_bwd_shard(const float* g_logprob, const float* g_entropy,
   if (v_lo < 0 || v_lo > 0x7fffff00LL) return fail(EAS_ERR_INVALID_ARG, "v_lo out of range");
   return bwd_impl(g_logprob, g_entropy, hidden, weight_shard, targets, mask, spans, num_spans, cap,
                   lse, entropy, T, H, V_shard, dtype, flags, vocab_chunk, dhidden_partial,
-                  dweight_shard, v_lo, true, ws, ws_bytes, stream);
+                  dweight_shard, v_lo, true, nullptr, ws, ws_bytes, stream);
 }
 
 eas_status eas_cp_local_layout(const uint8_t* mask, const int32_t* seg_offsets, int32_t n_segs,

@@ -198,6 +198,7 @@ struct RowScalars {
   float glp;
   int tgt;       // chunk-local target column, or -1 outside the chunk
   bool active;
+  float hs;      // e4m3 d-logits: scale of the row's quantised hidden
 };
 
 // TMA store of a shared-memory box to the map's coordinates (c0, c1), as one
@@ -232,6 +233,9 @@ __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* smem_dst, const CUtensorMap* map,
+                                                      uint32_t bar, int c0, int c1,
+                                                      uint64_t policy);
 // Coalesced row stores.  tcgen05.ld (32x32b) hands each lane one row of the
 // tile, so a lane storing its own row would touch 32 rows (32 memory lines)
 // per warp store.  octet_transpose regroups a chunk across each group of 8
@@ -262,8 +266,10 @@ __device__ __forceinline__ void octet_transpose(T (&x)[32], int i) {
 // - p) - g_H p (z - lse + H), p = exp(z - lse), written as -p (g_H (z - lse)
 // + g_lp + g_H H) + g_lp onehot.  Inactive rows and columns past the live
 // width are exact zeros.
+template <bool kScaled>
 __device__ __forceinline__ void dlogits_chunk(const TcJob& jb, uint32_t taddr, bool k_empty,
-                                              int col0, const RowScalars& rs, uint32_t* pk) {
+                                              int col0, const RowScalars& rs, uint32_t* pk,
+                                              const float* __restrict__ wsc) {
   // tcgen05.ld is warp-collective: only warp-uniform conditions (live width,
   // empty K) may skip it; per-row activity is applied afterwards.
   if (col0 >= jb.vc_live) {
@@ -285,6 +291,23 @@ __device__ __forceinline__ void dlogits_chunk(const TcJob& jb, uint32_t taddr, b
   }
   const int cvalid = jb.vc_live - col0;
   const int tj = rs.tgt - col0;
+  if constexpr (kScaled) {
+    // e4m3 operands: z = acc * scale(row) * scale(vocabulary row); wsc points
+    // at the scale of this chunk's column col0
+    if (cvalid >= 32 && (reinterpret_cast<uintptr_t>(wsc) & 15u) == 0) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 w4 = __ldg(reinterpret_cast<const float4*>(wsc) + q4);
+        v[4 * q4] *= rs.hs * w4.x;
+        v[4 * q4 + 1] *= rs.hs * w4.y;
+        v[4 * q4 + 2] *= rs.hs * w4.z;
+        v[4 * q4 + 3] *= rs.hs * w4.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= rs.hs * (j < cvalid ? __ldg(wsc + j) : 0.f);
+    }
+  }
   float d[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
@@ -314,17 +337,21 @@ __device__ __forceinline__ void dlogits_chunk(const TcJob& jb, uint32_t taddr, b
 // 128-byte swizzled layout (16-byte chunk j of row l at chunk j ^ (l & 7)),
 // and lane 0 writes the box with a TMA store.  Two boxes per warp alternate;
 // `cnt` counts the warp's boxes so far.
+template <bool kScaled>
 __device__ __forceinline__ void epi_dlogits(const TcJob& jb, uint32_t tbase, bool k_empty,
                                             long long r0, int n_blk, int row,
-                                            const RowScalars& rs, uint8_t* sEpi, uint32_t& cnt) {
+                                            const RowScalars& rs, uint8_t* sEpi, uint32_t& cnt,
+                                            const float* __restrict__ wscale) {
   const int n0 = n_blk * kTcBN;
   const int lane = row & 31;
   const int q = row >> 5;
 #pragma unroll 1
   for (int c = 0; c < kTcBN / 64; ++c) {
     uint32_t pk[32];
-    dlogits_chunk(jb, tbase + c * 64, k_empty, n0 + c * 64, rs, pk);
-    dlogits_chunk(jb, tbase + c * 64 + 32, k_empty, n0 + c * 64 + 32, rs, pk + 16);
+    const float* wsc = kScaled ? wscale + jb.v0 + n0 + c * 64 : nullptr;
+    dlogits_chunk<kScaled>(jb, tbase + c * 64, k_empty, n0 + c * 64, rs, pk, wsc);
+    dlogits_chunk<kScaled>(jb, tbase + c * 64 + 32, k_empty, n0 + c * 64 + 32, rs, pk + 16,
+                           kScaled ? wsc + 32 : nullptr);
     uint8_t* box = sEpi + ((cnt & 1u) * 4 + q) * 4096;
     if (lane == 0) bulk_wait_read<1>();     // the box's previous store has read it
     __syncwarp();
@@ -492,12 +519,12 @@ constexpr int kPKBlockBytes = kPHalf * 128;       // one 128-byte-swizzled k-blo
 // measured no better with them.
 template <int kMode>
 struct PipeGeo {
-  static constexpr int kSub = (kMode == 2) ? 2 : 1;
-  static constexpr int kStages = (kMode == 2) ? 3 : (kMode == 1) ? 6 : 7;
+  static constexpr int kSub = (kMode >= 2) ? 2 : 1;
+  static constexpr int kStages = (kMode >= 2) ? 3 : (kMode == 1) ? 6 : 7;
   static constexpr int kABytes = kSub * kPKBlockBytes;
   static constexpr int kBBytes = kSub * kPKBlockBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kEpiBytes = (kMode == 1) ? 32768 : 0;
+  static constexpr int kEpiBytes = (kMode == 1 || kMode == 3) ? 32768 : 0;
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024 + 512;
 };
 // the backward's MN-major operands come in TMA boxes of one k-block's 64
@@ -578,6 +605,22 @@ __device__ __forceinline__ void tma_load_3d_pair(void* smem_dst, const CUtensorM
       : "memory");
 }
 
+// The same load with an L2 eviction-priority hint (a createpolicy policy).
+// Only the bf16 forward uses it: its band of Hp rows is kept (evict-last)
+// while W streams past (evict-first), which cut its DRAM bytes on long_256k
+// from 181 to 155 GB and the step by 0.5 %.  The same hints on the backward
+// jobs added DRAM traffic, since the streamed operand is shared by the band's
+// tiles of one wave.
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* smem_dst, const CUtensorMap* map,
+                                                      uint32_t bar, int c0, int c1,
+                                                      uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "l"(policy)
+      : "memory");
+}
+
 // e4m3 k-block: 128 one-byte elements per 128-byte swizzle row.
 constexpr int kKbFp8 = 128;
 
@@ -625,12 +668,13 @@ __device__ __forceinline__ void umma_commit_pair_local(uint64_t* bar) {
 
 // One instantiation per family of jobs, so that each carries only the code
 // its jobs run (the kernel's size measurably costs throughput):
-//   kMode 0: bf16 forward (kTcFwd), 1: bf16 backward (kTcDLogits, kTcDHidden,
+//   kMode 0: bf16 forward (kTcFwd), 3: e4m3 d-logits (kTcDLogitsFp8, the e4m3
+//   backward's recompute), 1: bf16 backward (kTcDLogits, kTcDHidden,
 //   kTcDWeight), 2: e4m3 forward (kTcFwdFp8).
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_constant__ TcArgs a) {
-  constexpr bool kFp8 = (kMode == 2);
-  constexpr bool kFwd = (kMode != 1);
+  constexpr bool kFp8 = (kMode == 2 || kMode == 3);
+  constexpr bool kFwd = (kMode == 0 || kMode == 2);
   using G = PipeGeo<kMode>;
   constexpr int kPStages = G::kStages;
   constexpr int kPABytes = G::kABytes;
@@ -772,7 +816,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPStageBytes);
           constexpr int kblk = kFp8 ? kKbFp8 : kTcBK;      // K of one k-block
           const int k0 = kb * G::kSub * kblk;
-          if (kFwd || kind == kTcDLogits) {
+          if constexpr (kFwd && !kFp8) {
+            uint64_t keep, stream;
+            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
+            tma_load_2d_pair_hint(dA, &jb.tmA, bar, k0, mrow, keep);
+            tma_load_2d_pair_hint(dB, &jb.tmB, bar, k0, jb.v0 + ncol, stream);
+          } else if (kFwd || kMode == 3 || kind == kTcDLogits) {
 #pragma unroll
             for (int sb = 0; sb < G::kSub; ++sb) {
               tma_load_2d_pair(dA + sb * kPKBlockBytes, &jb.tmA, bar, k0 + sb * kblk, mrow);
@@ -817,8 +867,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         if (t < 0) break;
         const Work w = locate(t, js, a.n_jobs, a);
         const int kind = a.jobs[w.job].kind;
-        const bool a_mn = !kFwd && (kind == kTcDWeight);
-        const bool b_mn = !kFwd && (kind == kTcDHidden || kind == kTcDWeight);
+        const bool a_mn = (kMode == 1) && (kind == kTcDWeight);
+        const bool b_mn = (kMode == 1) && (kind == kTcDHidden || kind == kTcDWeight);
         const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPM, kTcBN)
                                     : a_mn ? idesc_bf16_f32(kPM, kTcBN, true, true)
                                     : (b_mn ? idesc_bf16_f32(kPM, kTcBN, false, true)
@@ -914,10 +964,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
           tgt = a.targets[tok] - a.t_off;
           if constexpr (kFp8) rscale = a.hscale[tok];
         }
-      } else if (kind == kTcDLogits) {
+      } else if (kMode == 3 || kind == kTcDLogits) {
         active = (tok >= 0) && (a.mask[tok] != 0);
         rs.active = active;
         if (active) {
+          if constexpr (kMode == 3) rs.hs = a.hscale[tok];
           const float l = a.lse[tok], h = a.ent[tok], gl = a.g_lp[tok], gh = a.g_h[tok];
           rs.lse2 = l * kLog2e;
           rs.gh2 = gh * kLn2;
@@ -935,12 +986,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       }
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
-      if constexpr (kFp8) {
+      if constexpr (kMode == 3) {
+        epi_dlogits<true>(jb, tbase, k_empty, r0, w.tc.n, row, rs, sEpi, epi_cnt, a.wscale);
+      } else if constexpr (kFp8) {
         epi_fwd<true>(a, tbase, k_empty, r0, w.tc.n, row, tgt, rscale, a.wscale);
       } else if constexpr (kFwd) {
         epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
       } else {
-        if (kind == kTcDLogits) epi_dlogits(jb, tbase, k_empty, r0, w.tc.n, row, rs, sEpi, epi_cnt);
+        if (kind == kTcDLogits)
+          epi_dlogits<false>(jb, tbase, k_empty, r0, w.tc.n, row, rs, sEpi, epi_cnt, nullptr);
         else if (kind == kTcDHidden) {
           if (jb.last_chunk) epi_dhidden_last(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
           else epi_dhidden_acc(a, jb, tbase, k_empty, r0, w.tc.n, row, sEpi, epi_cnt);
@@ -973,6 +1027,7 @@ size_t tc_smem_bytes() {
   size_t m = PipeGeo<0>::kSmemBytes;
   if (PipeGeo<1>::kSmemBytes > m) m = PipeGeo<1>::kSmemBytes;
   if (PipeGeo<2>::kSmemBytes > m) m = PipeGeo<2>::kSmemBytes;
+  if (PipeGeo<3>::kSmemBytes > m) m = PipeGeo<3>::kSmemBytes;
   return m;
 }
 
@@ -982,18 +1037,23 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   if (grid <= 0) return cudaSuccess;
   if (args.n_jobs < 1 || args.n_jobs > kMaxTcJobs) return cudaErrorInvalidValue;
   // the jobs of one launch belong to one family (see tc_pair_kernel)
-  auto family = [](int kind) { return kind == kTcFwd ? 0 : kind == kTcFwdFp8 ? 2 : 1; };
+  auto family = [](int kind) {
+    return kind == kTcFwd ? 0 : kind == kTcFwdFp8 ? 2 : kind == kTcDLogitsFp8 ? 3 : 1;
+  };
   const int mode = family(args.jobs[0].kind);
   for (int j = 1; j < args.n_jobs; ++j)
     if (family(args.jobs[j].kind) != mode) return cudaErrorInvalidValue;
   // the large dynamic shared memory is opted into once per device and
   // instantiation (one bit per device ordinal; a repeated opt-in is harmless)
-  static std::atomic<uint64_t> configured[3];
-  void (*kern)(TcArgs) = mode == 0 ? tc_pair_kernel<0> : mode == 1 ? tc_pair_kernel<1>
-                                                                    : tc_pair_kernel<2>;
-  const int smem = mode == 0 ? PipeGeo<0>::kSmemBytes
+  static std::atomic<uint64_t> configured[4];
+  void (*kern)(TcArgs) = mode == 0   ? tc_pair_kernel<0>
+                         : mode == 1 ? tc_pair_kernel<1>
+                         : mode == 2 ? tc_pair_kernel<2>
+                                     : tc_pair_kernel<3>;
+  const int smem = mode == 0   ? PipeGeo<0>::kSmemBytes
                    : mode == 1 ? PipeGeo<1>::kSmemBytes
-                               : PipeGeo<2>::kSmemBytes;
+                   : mode == 2 ? PipeGeo<2>::kSmemBytes
+                               : PipeGeo<3>::kSmemBytes;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;

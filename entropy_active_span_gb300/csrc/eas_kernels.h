@@ -56,6 +56,7 @@ enum TcKind : int {
   kTcDHidden = 2,  // dHacc (+)= dZ_c W_c -> fp32 accumulator / final dhidden
   kTcDWeight = 3,  // dW_c = dZ_c^T Hp -> fp32 dW rows
   kTcFwdFp8 = 4,   // as kTcFwd with e4m3 operands and per-row scales
+  kTcDLogitsFp8 = 5,  // as kTcDLogits with e4m3 operands and per-row scales
 };
 
 // One contraction of a launch.  A launch runs up to kMaxTcJobs jobs; their
@@ -107,8 +108,8 @@ struct TcArgs {
   void* dhidden;          // bf16 [T][H]
   int H;
   float* dW;              // fp32 [V][H]
-  const float* hscale;    // e4m3 forward: per-token scale of hidden [T]
-  const float* wscale;    // e4m3 forward: per-row scale of W [V]
+  const float* hscale;    // e4m3 kinds: per-token scale of hidden [T]
+  const float* wscale;    // e4m3 kinds: per-row scale of W [V]
 };
 
 size_t tc_smem_bytes();

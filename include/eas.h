@@ -72,8 +72,8 @@ typedef enum {
 typedef enum {
     EAS_BF16 = 0,   /* hidden, W, dhidden bf16; tensor cores, fp32 accumulate */
     EAS_FP32 = 1,   /* hidden, W, dhidden fp32; fp32 FMA throughout           */
-    EAS_E4M3 = 2    /* hidden, W in e4m3 with per-row fp32 scales; forward
-                       only (eas_lmhead_fwd_fp8), tensor cores             */
+    EAS_E4M3 = 2    /* hidden, W in e4m3 with per-row fp32 scales
+                       (eas_lmhead_fwd_fp8, eas_lmhead_bwd_fp8), tensor cores */
 } eas_dtype;
 
 /* Row policy for the forward/backward (the `flags` argument). */
@@ -221,7 +221,8 @@ eas_status eas_quantize_rows_e4m3(const void* src, eas_dtype src_dtype, int64_t 
  * and vocabulary row v is
  *   z = hidden_scale[t] * weight_scale[v] * sum_h e4m3(hidden[t,h]) e4m3(W[v,h])
  * accumulated in fp32 on the tensor cores (tcgen05 kind::f8f6f4); the rest is
- * eas_lmhead_fwd.  For forward-only scoring; the backward takes bf16 or fp32.
+ * eas_lmhead_fwd.  Used for forward-only scoring, and before eas_lmhead_bwd_fp8
+ * when training on e4m3 logits.
  * Requires H % 128 == 0.  Workspace: eas_lmhead_workspace_size(..., EAS_E4M3, 0).
  */
 eas_status eas_lmhead_fwd_fp8(const uint8_t* hidden_e4m3, const float* hidden_scale,
@@ -230,6 +231,41 @@ eas_status eas_lmhead_fwd_fp8(const uint8_t* hidden_e4m3, const float* hidden_sc
                               const int32_t* spans, const int32_t* num_spans, int64_t cap,
                               int64_t T, int64_t H, int64_t V, uint32_t flags,
                               float* logprob, float* entropy, float* lse,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward of the e4m3 forward (training with e4m3 logits).  The pages give
+ * no FP8 backward; this is the reading implemented here:
+ *   - the d-logits are those of the logits the e4m3 forward computes,
+ *       z' = hidden_scale[t] * weight_scale[v] * sum_h e4m3(hidden[t,h]) e4m3(W[v,h]),
+ *     recomputed on the tensor cores with the same e4m3 operands (kind::f8f6f4),
+ *     so they agree with the lse and entropy eas_lmhead_fwd_fp8 returned:
+ *       dZ' = g_lp (onehot - p') - g_H p' (z' - lse + H),  p' = exp(z' - lse);
+ *   - they are staged in bf16 and projected with the unquantised bf16
+ *     operands, as eas_lmhead_bwd does: dHidden = dZ' W, dW = dZ'^T hidden.
+ * Each vocabulary chunk is two launches: the e4m3 d-logits, then dW and
+ * dHidden.
+ *
+ *   hidden, weight [T, H] / [V, H] bf16 : the unquantised operands
+ *   hidden_e4m3, hidden_scale, weight_e4m3, weight_scale : the same operands
+ *            quantised by eas_quantize_rows_e4m3 (as passed to the forward)
+ *   lse, entropy [T] fp32 : eas_lmhead_fwd_fp8's outputs for these operands
+ * Other arguments and outputs are those of eas_lmhead_bwd (dtype bf16).  The
+ * backward packs its own rows: EAS_REUSE_FWD_ROWS is rejected.  Requires
+ * H % 128 == 0.  Workspace: eas_lmhead_bwd_fp8_workspace_size(T, H, V,
+ * vocab_chunk) bytes.
+ */
+size_t eas_lmhead_bwd_fp8_workspace_size(int64_t T, int64_t H, int64_t V, int64_t vocab_chunk);
+
+eas_status eas_lmhead_bwd_fp8(const float* g_logprob, const float* g_entropy,
+                              const void* hidden, const void* weight,
+                              const uint8_t* hidden_e4m3, const float* hidden_scale,
+                              const uint8_t* weight_e4m3, const float* weight_scale,
+                              const int32_t* targets, const uint8_t* mask,
+                              const int32_t* spans, const int32_t* num_spans, int64_t cap,
+                              const float* lse, const float* entropy,
+                              int64_t T, int64_t H, int64_t V, uint32_t flags,
+                              int64_t vocab_chunk, void* dhidden, float* dweight,
                               void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------ vocabulary-parallel path */

@@ -8,7 +8,7 @@ import torch
 
 import entropy_active_span_gb300 as eas
 from entropy_active_span_gb300 import workloads as W
-from gpu_helpers import BF16_TOL, small_inputs, to_dev
+from gpu_helpers import BF16_TOL, rel_fro, small_inputs, to_dev
 import oracle
 
 pytestmark = pytest.mark.gpu
@@ -101,3 +101,119 @@ def test_fp8_forward_full_size_rl_16k():
     assert np.max(np.abs(lp[idx].cpu().numpy() - rlp)) <= BF16_TOL["lp"]
     assert np.max(np.abs(ent[idx].cpu().numpy() - rent)) <= BF16_TOL["ent"]
     assert np.max(np.abs(lse[idx].cpu().numpy() - rlse)) <= BF16_TOL["lp"]
+
+
+# ------------------------------------------------------------- backward
+#
+# eas_lmhead_bwd_fp8: d-logits of the e4m3 logits (recomputed from the same
+# e4m3 operands the forward used), projected with the bf16 operands.  The
+# oracle is oracle.lmhead_backward_e4m3 (it quantises its own operands; its
+# codes equal the device's, test_quantizer_bit_exact), pinned on the CPU to
+# the bf16 oracle by the special cases in test_oracle_fp8.py.
+
+def _fp8_step(inp, chunk=0, flags=eas.EAS_ROWS_ACTIVE):
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    glp, gh = to_dev(inp["g_logprob"]), to_dev(inp["g_entropy"])
+    h8, hs = eas.quantize_rows_e4m3(h)
+    w8, wsc = eas.quantize_rows_e4m3(w)
+    spans, ns = eas.build_active_spans(m, 128)
+    lp, ent, lse = eas.lmhead_fwd_fp8(h8, hs, w8, wsc, t, m, spans, ns, flags)
+    ws = eas.workspace(eas.lmhead_bwd_fp8_workspace_size(*h.shape, w.shape[0], chunk), h.device)
+    dh, dw = eas.lmhead_bwd_fp8(glp, gh, h, w, h8, hs, w8, wsc, t, m, spans, ns, lse, ent, flags,
+                                chunk, ws=ws)
+    assert eas.read_device_status(ws) == 0
+    torch.cuda.synchronize()
+    return dh.float().cpu().numpy(), dw.cpu().numpy()
+
+
+@pytest.mark.parametrize("T,H,V,chunk,kind,w_std,flags", [
+    (700, 256, 1000, 0, "bernoulli0.6", 3.0, eas.EAS_ROWS_ACTIVE),
+    (700, 256, 1000, 384, "bernoulli0.6", 3.0, eas.EAS_ROWS_ACTIVE),
+    (300, 128, 257, 0, "bernoulli0.9", 8.0, eas.EAS_ROWS_SPAN),
+    (2048, 512, 5000, 1537, "sparse_short", 2.0, eas.EAS_ROWS_ACTIVE),
+    (1000, 384, 3000, 1000, "bernoulli0.5", 1.0, eas.EAS_ROWS_SPAN),
+])
+def test_fp8_backward_matches_oracle(T, H, V, chunk, kind, w_std, flags):
+    inp = small_inputs(T, H, V, seed=T + V + chunk, mask_kind=kind, w_std=w_std)
+    dh, dw = _fp8_step(inp, chunk, flags)
+    rdh, rdw = oracle.lmhead_backward_e4m3(W.to_f64(inp["hidden"]), W.to_f64(inp["weight"]),
+                                           inp["targets"], inp["mask"], inp["g_logprob"],
+                                           inp["g_entropy"])
+    assert rel_fro(dh, rdh) <= BF16_TOL["fro"]
+    assert rel_fro(dw, rdw) <= BF16_TOL["fro"]
+    inactive = inp["mask"] == 0
+    assert np.all(dh[inactive] == 0)
+
+
+def test_fp8_backward_is_the_e4m3_gradient_not_the_bf16_one():
+    """With logits of std ~5 the e4m3 and bf16 gradients differ by about 4 %
+    (relative Frobenius), four times the tolerance: the result must match the
+    e4m3 oracle and miss the bf16 one, so a recompute that silently ran on the
+    bf16 operands would fail."""
+    inp = small_inputs(512, 512, 2048, seed=77, mask_kind="bernoulli0.6", w_std=10.0)
+    dh, dw = _fp8_step(inp, 1024)
+    args = (W.to_f64(inp["hidden"]), W.to_f64(inp["weight"]), inp["targets"], inp["mask"],
+            inp["g_logprob"], inp["g_entropy"])
+    rdh, rdw = oracle.lmhead_backward_e4m3(*args)
+    bdh, bdw = oracle.lmhead_backward(*args)
+    assert rel_fro(rdh, bdh) > 3 * BF16_TOL["fro"]
+    assert rel_fro(dh, rdh) <= BF16_TOL["fro"] and rel_fro(dw, rdw) <= BF16_TOL["fro"]
+    assert rel_fro(dh, bdh) > 2 * BF16_TOL["fro"] and rel_fro(dw, bdw) > 2 * BF16_TOL["fro"]
+
+
+def test_fp8_backward_is_deterministic():
+    inp = small_inputs(1000, 256, 1000, seed=5, mask_kind="bernoulli0.6", w_std=4.0)
+    a = _fp8_step(inp, 384)
+    b = _fp8_step(inp, 384)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+def test_fp8_backward_rejects_forward_row_reuse():
+    inp = small_inputs(256, 128, 512, seed=6)
+    h, w = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    g = to_dev(inp["g_logprob"])
+    h8, hs = eas.quantize_rows_e4m3(h)
+    w8, wsc = eas.quantize_rows_e4m3(w)
+    spans, ns = eas.build_active_spans(m, 128)
+    lp, ent, lse = eas.lmhead_fwd_fp8(h8, hs, w8, wsc, t, m, spans, ns)
+    with pytest.raises(eas.EasError):
+        eas.lmhead_bwd_fp8(g, g, h, w, h8, hs, w8, wsc, t, m, spans, ns, lse, ent,
+                           eas.EAS_REUSE_FWD_ROWS)
+
+
+def test_fp8_backward_full_size_rl_16k():
+    """The e4m3 backward at the rl_16k shape with a peaked W: dHidden on
+    sampled rows, and the whole dW from a second backward whose upstream
+    gradients vanish outside a row sample S."""
+    w = W.WORKLOADS["rl_16k"]
+    inp = W.make_inputs(w, w_std=1.5)
+    h, wt = to_dev(inp["hidden"]), to_dev(inp["weight"])
+    t, m = to_dev(inp["targets"]), to_dev(inp["mask"])
+    h8, hs = eas.quantize_rows_e4m3(h)
+    w8, wsc = eas.quantize_rows_e4m3(wt)
+    spans, ns = eas.build_active_spans(m, 128)
+    lp, ent, lse = eas.lmhead_fwd_fp8(h8, hs, w8, wsc, t, m, spans, ns)
+    ws = eas.workspace(eas.lmhead_bwd_fp8_workspace_size(w.T, w.H, w.V), h.device)
+    act = np.flatnonzero(inp["mask"])
+    rng = np.random.default_rng(w.seed)
+    S = np.unique(np.concatenate([act[:2], act[-2:], rng.choice(act, 48, replace=False)]))
+    g1 = np.zeros(w.T, np.float32)
+    g2 = np.zeros(w.T, np.float32)
+    g1[S] = inp["g_logprob"][S]
+    g2[S] = inp["g_entropy"][S]
+    dh, dw = eas.lmhead_bwd_fp8(to_dev(g1), to_dev(g2), h, wt, h8, hs, w8, wsc, t, m, spans, ns,
+                                lse, ent, ws=ws)
+    assert eas.read_device_status(ws) == 0
+    W64 = W.to_f64(inp["weight"])
+    Wq = oracle.dequantized_rows(W64)
+    rdh, rdw = oracle.lmhead_backward_e4m3_rows_weighted(W.to_f64(inp["hidden"][S]), W64, Wq,
+                                                         inp["targets"][S], g1[S], g2[S])
+    idx = torch.from_numpy(S).cuda()
+    assert rel_fro(dh[idx].float().cpu().numpy(), rdh) <= BF16_TOL["fro"]
+    assert rel_fro(dw.cpu().numpy(), rdw) <= BF16_TOL["fro"]
+    others = torch.ones(w.T, dtype=torch.bool, device="cuda")
+    others[idx] = False
+    assert torch.all(dh[others] == 0)
