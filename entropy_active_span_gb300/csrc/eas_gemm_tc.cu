@@ -704,26 +704,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
   const Sched* sched = static_cast<const Sched*>(a.sched);
   DevStatus* st = static_cast<DevStatus*>(a.status);
 
-  JobShape js[kMaxTcJobs];
-  int total = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxTcJobs; ++j) {
-    js[j] = JobShape{0, 0, 0, 0, total};
-    if (j < a.n_jobs) {
-      const TcJob& jb = a.jobs[j];
-      const int M = jb.M_fixed > 0 ? jb.M_fixed : sched->R_pad;
-      // a reduction over packed rows (dW) stops at the last k-block holding a
-      // real row; rows from R to R_pad are zero in both operands
-      const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R;
-      js[j].num_m = (M + kPM - 1) / kPM;
-      js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
-      constexpr int kse = G::kSub * (kFp8 ? kKbFp8 : kTcBK);   // K per stage
-      js[j].num_kb = (K + kse - 1) / kse;
-      js[j].tiles = js[j].num_m * js[j].num_n;
-      total += js[j].tiles;
-    }
-  }
-
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(&full[i], 1);
@@ -759,6 +739,36 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
   cluster_sync_all();     // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+
+  // Launched with programmatic stream serialisation, the prologue above may
+  // run while the previous kernel of the stream finishes; nothing it touched
+  // is that kernel's output.  Every read of global memory comes after this
+  // wait, which returns once the previous grid has completed and its writes
+  // are visible (and at once for a launch without the attribute).  Dependents
+  // are then released: their CTAs find a free SM only when a CTA of this grid
+  // exits (one CTA per SM), and wait here in turn.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+  JobShape js[kMaxTcJobs];
+  int total = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTcJobs; ++j) {
+    js[j] = JobShape{0, 0, 0, 0, total};
+    if (j < a.n_jobs) {
+      const TcJob& jb = a.jobs[j];
+      const int M = jb.M_fixed > 0 ? jb.M_fixed : sched->R_pad;
+      // a reduction over packed rows (dW) stops at the last k-block holding a
+      // real row; rows from R to R_pad are zero in both operands
+      const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R;
+      js[j].num_m = (M + kPM - 1) / kPM;
+      js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
+      constexpr int kse = G::kSub * (kFp8 ? kKbFp8 : kTcBK);   // K per stage
+      js[j].num_kb = (K + kse - 1) / kse;
+      js[j].tiles = js[j].num_m * js[j].num_n;
+      total += js[j].tiles;
+    }
+  }
 
   // shared::cluster addresses of the leader's barriers and the peer's ring
   const uint32_t full_leader0 = map_rank(&full[0], 0);
@@ -1070,13 +1080,18 @@ cudaError_t launch_tc_gemm(const TcArgs& args, int grid, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the CTA prologue (barrier set-up, TMEM
+  // allocation, descriptor prefetch) overlaps the previous kernel's last
+  // wave; the kernel waits for that grid before its first global read
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, args);
 }
 
