@@ -29,7 +29,11 @@
 // k-block, an MN-major one (dHidden's B, dW's A and B) in one 3-D box
 // {64 columns, 64 k-rows, 2 column blocks}, so the producer issues two TMA
 // instructions per k-block whatever the kind.  Each CTA's TMEM receives its
-// 128 x 256 half of the accumulator.  CTA
+// 128 x 256 half of the accumulator.  When the last m-tile of a job over the
+// packed rows holds at most 128 real rows, the bf16 backward instantiation
+// (d-logits, dHidden) computes it as a 128 x 256 pair MMA (64 rows per CTA,
+// half the tensor time) instead of carrying the padding rows through the
+// tensor pipe; its results are bit-identical to those of a full tile.  CTA
 // layout (192 threads): warp 0 = TMA producer (lane 0; on the even CTA it also
 // fetches tile indices and publishes them to both CTAs), warp 1 = MMA issuer
 // (lane 0 of the even CTA) and TMEM owner, warps 2..5 = epilogue, one
@@ -335,18 +339,18 @@ __device__ __forceinline__ void dlogits_chunk(const TcJob& jb, uint32_t taddr, b
 // d-logits tile rows into the bf16 staging buffer, 64 columns (128 bytes of a
 // row) per round: the warp's 32 rows go to a 4 KB shared-memory box in the
 // 128-byte swizzled layout (16-byte chunk j of row l at chunk j ^ (l & 7)),
-// and lane 0 writes the box with a TMA store.  Two boxes per warp alternate;
-// `cnt` counts the warp's boxes so far.
+// and lane 0 writes the box with a TMA store.  Two boxes per warp (q = warp
+// quadrant) alternate; `cnt` counts the warp's boxes so far.  The warp covers
+// tile columns [c0, c0 + ncol) of rows r0 + (row & ~31) .. + 31.
 template <bool kScaled>
 __device__ __forceinline__ void epi_dlogits(const TcJob& jb, uint32_t tbase, bool k_empty,
-                                            long long r0, int n_blk, int row,
-                                            const RowScalars& rs, uint8_t* sEpi, uint32_t& cnt,
-                                            const float* __restrict__ wscale) {
-  const int n0 = n_blk * kTcBN;
+                                            long long r0, int n_blk, int q, int row, int c0,
+                                            int ncol, const RowScalars& rs, uint8_t* sEpi,
+                                            uint32_t& cnt, const float* __restrict__ wscale) {
+  const int n0 = n_blk * kTcBN + c0;
   const int lane = row & 31;
-  const int q = row >> 5;
 #pragma unroll 1
-  for (int c = 0; c < kTcBN / 64; ++c) {
+  for (int c = 0; c < ncol / 64; ++c) {
     uint32_t pk[32];
     const float* wsc = kScaled ? wscale + jb.v0 + n0 + c * 64 : nullptr;
     dlogits_chunk<kScaled>(jb, tbase + c * 64, k_empty, n0 + c * 64, rs, pk, wsc);
@@ -362,7 +366,7 @@ __device__ __forceinline__ void epi_dlogits(const TcJob& jb, uint32_t tbase, boo
           make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) tma_store_2d(&jb.tmD, box, n0 + c * 64, static_cast<int>(r0) + q * 32);
+    if (lane == 0) tma_store_2d(&jb.tmD, box, n0 + c * 64, static_cast<int>(r0) + (row & ~31));
     ++cnt;
   }
 }
@@ -374,13 +378,13 @@ __device__ __forceinline__ void epi_dlogits(const TcJob& jb, uint32_t tbase, boo
 // element receives one add per launch, in chunk order across launches, so
 // the sum is deterministic.
 __device__ __forceinline__ void epi_dhidden_acc(const TcArgs& a, const TcJob& jb, uint32_t tbase,
-                                                bool k_empty, long long r0, int n_blk, int row,
-                                                uint8_t* sEpi, uint32_t& cnt) {
-  const int n0 = n_blk * kTcBN;
+                                                bool k_empty, long long r0, int n_blk, int q,
+                                                int row, int c0, int ncol, uint8_t* sEpi,
+                                                uint32_t& cnt) {
+  const int n0 = n_blk * kTcBN + c0;
   const int lane = row & 31;
-  const int q = row >> 5;
 #pragma unroll 1
-  for (int c = 0; c < kTcBN / 32; ++c) {
+  for (int c = 0; c < ncol / 32; ++c) {
     if (n0 + c * 32 >= a.H) break;
     float v[32];
     if (k_empty) {
@@ -400,8 +404,9 @@ __device__ __forceinline__ void epi_dhidden_acc(const TcArgs& a, const TcJob& jb
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      if (jb.first_chunk) tma_store_2d(&jb.tmD, box, n0 + c * 32, static_cast<int>(r0) + q * 32);
-      else tma_reduce_add_2d(&jb.tmD, box, n0 + c * 32, static_cast<int>(r0) + q * 32);
+      const int rr = static_cast<int>(r0) + (row & ~31);
+      if (jb.first_chunk) tma_store_2d(&jb.tmD, box, n0 + c * 32, rr);
+      else tma_reduce_add_2d(&jb.tmD, box, n0 + c * 32, rr);
     }
     ++cnt;
   }
@@ -411,9 +416,9 @@ __device__ __forceinline__ void epi_dhidden_acc(const TcArgs& a, const TcJob& jb
 // accumulator (unless it is also the first chunk), converted to bf16 and
 // scattered to the rows' tokens (zeros for gap rows whose mask byte is 0).
 __device__ __forceinline__ void epi_dhidden_last(const TcArgs& a, const TcJob& jb, uint32_t tbase,
-                                            bool k_empty, long long r0, int n_blk, int row, int tok,
-                                            bool active) {
-  const int n0 = n_blk * kTcBN;
+                                            bool k_empty, long long r0, int n_blk, int row, int c0,
+                                            int ncol, int tok, bool active) {
+  const int n0 = n_blk * kTcBN + c0;
   const int lane = row & 31;
   const int i = lane & 7;
   const long long r_oct = r0 + (row & ~31) + (lane & ~7);
@@ -428,7 +433,7 @@ __device__ __forceinline__ void epi_dhidden_last(const TcArgs& a, const TcJob& j
     if (__shfl_sync(0xffffffffu, active ? 1 : 0, (lane & ~7) + p)) act_bits |= 1u << p;
   }
 #pragma unroll 1
-  for (int c = 0; c < kTcBN / 32; ++c) {
+  for (int c = 0; c < ncol / 32; ++c) {
     if (n0 + c * 32 >= a.H) break;
     float v[32];
     if (k_empty) {
@@ -525,6 +530,8 @@ struct PipeGeo {
   static constexpr int kBBytes = kSub * kPKBlockBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiBytes = (kMode == 1 || kMode == 3) ? 32768 : 0;
+  // 128-row last m-tiles: the bf16 backward kinds (d-logits, dHidden)
+  static constexpr bool kHalfTiles = (kMode == 1);
   static constexpr int kSmemBytes = kStages * kStageBytes + kEpiBytes + 1024 + 512;
 };
 // the backward's MN-major operands come in TMA boxes of one k-block's 64
@@ -769,6 +776,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       total += js[j].tiles;
     }
   }
+  // The last m-tile of the jobs over the packed rows (M = R_pad) holds at most
+  // 128 real rows: the backward instantiation runs it as a 128-row tile.
+  bool last_half = false;
+  if constexpr (G::kHalfTiles) {
+    const int last = sched->R - (sched->R_pad / kPM - 1) * kPM;
+    last_half = last > 0 && last <= kPHalf;
+  }
 
   // shared::cluster addresses of the leader's barriers and the peer's ring
   const uint32_t full_leader0 = map_rank(&full[0], 0);
@@ -812,7 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         const Work w = locate(t, js, a.n_jobs, a);
         const TcJob& jb = a.jobs[w.job];
         const int kind = jb.kind;
-        const int mrow = w.tc.m * kPM + static_cast<int>(rank) * kPHalf;   // this CTA's A rows
+        // a 128-row tile: each CTA's A operand is 64 rows (the box still
+        // loads 128, of which the MMA reads the first 64)
+        const bool half = last_half && a.jobs[w.job].M_fixed <= 0 && w.tc.m == js[w.job].num_m - 1;
+        const int mrow = w.tc.m * kPM + static_cast<int>(rank) * (half ? kPHalf / 2 : kPHalf);
         const int ncol = w.tc.n * kTcBN + static_cast<int>(rank) * kPHalf; // this CTA's B columns
         for (int kb = 0; kb < js[w.job].num_kb; ++kb) {
           if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
@@ -879,10 +896,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         const int kind = a.jobs[w.job].kind;
         const bool a_mn = (kMode == 1) && (kind == kTcDWeight);
         const bool b_mn = (kMode == 1) && (kind == kTcDHidden || kind == kTcDWeight);
+        const bool half = last_half && a.jobs[w.job].M_fixed <= 0 && w.tc.m == js[w.job].num_m - 1;
+        const int mm = half ? kPHalf : kPM;
         const uint32_t idesc = kFp8 ? idesc_e4m3_f32(kPM, kTcBN)
                                     : a_mn ? idesc_bf16_f32(kPM, kTcBN, true, true)
-                                    : (b_mn ? idesc_bf16_f32(kPM, kTcBN, false, true)
-                                            : idesc_bf16_f32(kPM, kTcBN, false, false));
+                                    : (b_mn ? idesc_bf16_f32(mm, kTcBN, false, true)
+                                            : idesc_bf16_f32(mm, kTcBN, false, false));
         const uint32_t a_lbo = a_mn ? 8192 : 16, a_step = a_mn ? 2048 : 32;
         const uint32_t b_lbo = b_mn ? 8192 : 16, b_step = b_mn ? 2048 : 32;
         const int buf = it & 1;
@@ -939,7 +958,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
   } else {
     // ------------------------------------------------ epilogue warps (both CTAs)
     const int q = warp & 3;
-    const int row = q * 32 + lane;
     uint32_t epi_cnt = 0;
     for (int it = 0;; ++it) {
       const int slot = it % kRing;
@@ -960,7 +978,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       const bool k_empty = (js[w.job].num_kb == 0);
       const int buf = it & 1;
       const uint32_t tph = (it >> 1) & 1;
-      const long long r0 = static_cast<long long>(w.tc.m) * kPM + static_cast<long long>(rank) * kPHalf;
+      // Rows and columns this warp holds.  A 256-row tile gives CTA r rows
+      // [128r, 128r + 128), TMEM lane = row.  A 128-row tile (the last m-tile
+      // of a job with at most 128 real rows there, computed by a 128 x 256
+      // pair MMA) gives CTA r rows [64r, 64r + 64): TMEM lanes 0..63 hold
+      // their columns 0..127 and lanes 64..127 the same rows' columns 128..255.
+      const bool half = last_half && a.jobs[w.job].M_fixed <= 0 && w.tc.m == js[w.job].num_m - 1;
+      const int hcol = half ? (q >> 1) : 0;
+      const int row = (half ? (q & 1) : q) * 32 + lane;
+      const int c0 = hcol * (kTcBN / 2);
+      const int ncol = half ? kTcBN / 2 : kTcBN;
+      const long long r0 = static_cast<long long>(w.tc.m) * kPM +
+                           static_cast<long long>(rank) * (half ? kPHalf / 2 : kPHalf);
       const long long r = r0 + row;
       int tok = -1;
       if (kind != kTcDWeight) tok = a.row_map[r];
@@ -997,17 +1026,21 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
       if constexpr (kMode == 3) {
-        epi_dlogits<true>(jb, tbase, k_empty, r0, w.tc.n, row, rs, sEpi, epi_cnt, a.wscale);
+        epi_dlogits<true>(jb, tbase, k_empty, r0, w.tc.n, q, row, c0, ncol, rs, sEpi, epi_cnt,
+                          a.wscale);
       } else if constexpr (kFp8) {
         epi_fwd<true>(a, tbase, k_empty, r0, w.tc.n, row, tgt, rscale, a.wscale);
       } else if constexpr (kFwd) {
         epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
       } else {
         if (kind == kTcDLogits)
-          epi_dlogits<false>(jb, tbase, k_empty, r0, w.tc.n, row, rs, sEpi, epi_cnt, nullptr);
+          epi_dlogits<false>(jb, tbase, k_empty, r0, w.tc.n, q, row, c0, ncol, rs, sEpi, epi_cnt,
+                             nullptr);
         else if (kind == kTcDHidden) {
-          if (jb.last_chunk) epi_dhidden_last(a, jb, tbase, k_empty, r0, w.tc.n, row, tok, active);
-          else epi_dhidden_acc(a, jb, tbase, k_empty, r0, w.tc.n, row, sEpi, epi_cnt);
+          if (jb.last_chunk)
+            epi_dhidden_last(a, jb, tbase, k_empty, r0, w.tc.n, row, c0, ncol, tok, active);
+          else
+            epi_dhidden_acc(a, jb, tbase, k_empty, r0, w.tc.n, q, row, c0, ncol, sEpi, epi_cnt);
         }
         else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
       }

@@ -157,6 +157,26 @@ def test_active_rows_match_the_dense_mask_run(dtype):
         np.testing.assert_array_equal(sparse[k][act], dense[k][act])
 
 
+@pytest.mark.parametrize("R", [1, 64, 127, 128, 129, 255, 256, 257, 300, 383, 384, 385, 511])
+def test_last_row_tile_of_at_most_128_rows(R):
+    """When the last 256-row tile holds at most 128 real rows it runs as a
+    128 x 256 pair MMA (forward, d-logits, dHidden).  R active tokens, drawn
+    from tokens 0..511: the results match the oracle, and every active row is
+    bit-identical to the same token in the dense-mask run, where tokens
+    0..511 all sit in full 256-row tiles."""
+    T, H, V = 600, 256, 700
+    rng = np.random.default_rng(4000 + R)
+    mask = np.zeros(T, np.uint8)
+    mask[rng.choice(512, size=R, replace=False)] = 1
+    inp = small_inputs(T, H, V, seed=77, mask=mask, w_std=3.0)
+    got = run_gpu(inp, vocab_chunk=512)                 # chunks 512 and 188
+    check(got, oracle_all(inp), inp["mask"], BF16_TOL)
+    dense = run_gpu(dict(inp, mask=np.ones(T, np.uint8)), vocab_chunk=512)
+    act = mask != 0
+    for k in ("logprob", "entropy", "lse", "dhidden"):
+        np.testing.assert_array_equal(got[k][act], dense[k][act])
+
+
 @pytest.mark.parametrize("T,H,V", [(300, 192, 300), (513, 320, 1000), (1, 64, 50), (257, 448, 2049)])
 def test_bf16_hidden_width_not_a_tile_multiple(T, H, V):
     """H % 256 != 0 leaves a partial N tile in dHidden and dW; T = 1 is a
