@@ -79,6 +79,7 @@ __device__ __forceinline__ TileCoord raster(int t, int num_m, int num_n, int gro
 // Per-job extents, identical in every thread.
 struct JobShape {
   int num_m, num_n, num_kb, tiles, first;
+  int num_nb;      // 256-column blocks of N (a wide tile's half h is block 2n + h)
 };
 
 struct Work {
@@ -516,18 +517,32 @@ constexpr int kPM = 256;                          // rows of a pair tile
 constexpr int kPKBlockBytes = kPHalf * 128;       // one 128-byte-swizzled k-block: 16 KB
 
 // Pipeline stage geometry of an instantiation.  A stage holds kSub k-blocks
-// of each operand.  The bf16 forward uses seven stages of one k-block (32 KB
-// per CTA); the backward six, leaving 32 KB for the epilogues' TMA staging
-// (two 4 KB boxes per epilogue warp).  The e4m3 forward, whose MMAs finish a
-// k-block in half the time, uses three stages of two k-blocks (64 KB): half
-// as many stage boundaries per unit of work, 2 % faster there, while bf16
-// measured no better with them.
+// of each operand.  The backward keeps 32 KB for the epilogues' TMA staging
+// (two 4 KB boxes per epilogue warp).  The e4m3 instantiations, whose MMAs
+// finish a k-block in half the time, compute 256 x 256 tiles in three stages
+// of two k-blocks (64 KB): half as many stage boundaries per unit of work.
+//
+// The bf16 backward instantiation computes 256 x 512 tiles ("wide"): a stage
+// holds one k-block of A and of both 256-column halves of B (48 KB per CTA,
+// four stages), and the two halves accumulate in TMEM columns [0, 256) and
+// [256, 512).  A 256 x 256 tile needs 32 KB per CTA per 512-cycle k-block,
+// 64 B per SM-clock, about what an SM takes in; sharing each A stage between
+// two halves brings that to 24 KB per half-tile's k-block, and the operand
+// traffic's power goes to the clock.  The halves run staggered: half 0 alone
+// for its first kWideStagger k-blocks, then both, then half 1 alone for its
+// first kWideStagger k-blocks.  Half 0's epilogue then runs under half 1's
+// last k-blocks and half 1's under the next tile's first ones, as the two
+// TMEM buffers of a 256 x 256 tile would.
+constexpr int kWideStagger = 16;   // k-blocks each half of a wide tile runs alone
+
 template <int kMode>
 struct PipeGeo {
+  static constexpr bool kWide = (kMode == 1);
+  static constexpr int kTileN = kWide ? 2 * kTcBN : kTcBN;
   static constexpr int kSub = (kMode >= 2) ? 2 : 1;
-  static constexpr int kStages = (kMode >= 2) ? 3 : (kMode == 1) ? 6 : 7;
+  static constexpr int kStages = (kMode >= 2) ? 3 : kWide ? 4 : 7;
   static constexpr int kABytes = kSub * kPKBlockBytes;
-  static constexpr int kBBytes = kSub * kPKBlockBytes;
+  static constexpr int kBBytes = (kWide ? 2 : 1) * kSub * kPKBlockBytes;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiBytes = (kMode == 1 || kMode == 3) ? 32768 : 0;
   // 128-row last m-tiles: the bf16 backward kinds (d-logits, dHidden)
@@ -761,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
   int total = 0;
 #pragma unroll
   for (int j = 0; j < kMaxTcJobs; ++j) {
-    js[j] = JobShape{0, 0, 0, 0, total};
+    js[j] = JobShape{0, 0, 0, 0, total, 0};
     if (j < a.n_jobs) {
       const TcJob& jb = a.jobs[j];
       const int M = jb.M_fixed > 0 ? jb.M_fixed : sched->R_pad;
@@ -769,7 +784,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       // real row; rows from R to R_pad are zero in both operands
       const int K = jb.K_fixed > 0 ? jb.K_fixed : sched->R;
       js[j].num_m = (M + kPM - 1) / kPM;
-      js[j].num_n = (jb.N + kTcBN - 1) / kTcBN;
+      js[j].num_n = (jb.N + G::kTileN - 1) / G::kTileN;
+      js[j].num_nb = (jb.N + kTcBN - 1) / kTcBN;
       constexpr int kse = G::kSub * (kFp8 ? kKbFp8 : kTcBK);   // K per stage
       js[j].num_kb = (K + kse - 1) / kse;
       js[j].tiles = js[j].num_m * js[j].num_n;
@@ -830,42 +846,105 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         // loads 128, of which the MMA reads the first 64)
         const bool half = last_half && a.jobs[w.job].M_fixed <= 0 && w.tc.m == js[w.job].num_m - 1;
         const int mrow = w.tc.m * kPM + static_cast<int>(rank) * (half ? kPHalf / 2 : kPHalf);
-        const int ncol = w.tc.n * kTcBN + static_cast<int>(rank) * kPHalf; // this CTA's B columns
-        for (int kb = 0; kb < js[w.job].num_kb; ++kb) {
-          if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
-            report(st, kStTimeout, 13, t);
-            ok = false;
-            break;
-          }
-          uint8_t* dA = sA + stage * kPABytes;
-          uint8_t* dB = sB + stage * kPBBytes;
-          const uint32_t bar = full_leader0 + 8 * stage;
-          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPStageBytes);
-          constexpr int kblk = kFp8 ? kKbFp8 : kTcBK;      // K of one k-block
-          const int k0 = kb * G::kSub * kblk;
-          if constexpr (kFwd && !kFp8) {
-            uint64_t keep, stream;
-            asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
-            asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
-            tma_load_2d_pair_hint(dA, &jb.tmA, bar, k0, mrow, keep);
-            tma_load_2d_pair_hint(dB, &jb.tmB, bar, k0, jb.v0 + ncol, stream);
-          } else if (kFwd || kMode == 3 || kind == kTcDLogits) {
-#pragma unroll
-            for (int sb = 0; sb < G::kSub; ++sb) {
-              tma_load_2d_pair(dA + sb * kPKBlockBytes, &jb.tmA, bar, k0 + sb * kblk, mrow);
-              tma_load_2d_pair(dB + sb * kPKBlockBytes, &jb.tmB, bar, k0 + sb * kblk,
-                               jb.v0 + ncol);
+        if constexpr (G::kWide) {
+          // k-steps of a wide tile: half 0 alone for k-blocks [0, js), both
+          // halves for [js, Kb), half 1 alone for [0, js); a tile whose second
+          // half lies past N runs half 0 only
+          const int Kb = js[w.job].num_kb;
+          const bool has1 = 2 * w.tc.n + 1 < js[w.job].num_nb;
+          const int jst = Kb < kWideStagger ? Kb : kWideStagger;
+          const int S = has1 ? Kb + jst : Kb;
+          const int ncol0 = w.tc.n * G::kTileN + static_cast<int>(rank) * kPHalf;
+          for (int sidx = 0; sidx < S; ++sidx) {
+            const int kb = sidx < Kb ? sidx : sidx - Kb;
+            const uint32_t hm = !has1 ? 1u : (sidx < jst ? 1u : (sidx < Kb ? 3u : 2u));
+            if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
+              report(st, kStTimeout, 13, t);
+              ok = false;
+              break;
             }
-          } else if (kind == kTcDHidden) {
-            tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
-            tma_load_3d_pair(dB, &jb.tmB, bar, 0, jb.v0 + k0, ncol >> 6);
-          } else {
-            tma_load_3d_pair(dA, &jb.tmA, bar, 0, k0, mrow >> 6);
-            tma_load_3d_pair(dB, &jb.tmB, bar, 0, k0, ncol >> 6);
+            uint8_t* dA = sA + stage * kPABytes;
+            uint8_t* dB = sB + stage * kPBBytes;
+            const uint32_t bar = full_leader0 + 8 * stage;
+            const uint32_t nbh = (hm == 3u) ? 2u : 1u;
+            if (leader)
+              mbar_arrive_expect_tx(&full[stage], 2u * (kPABytes + nbh * kPKBlockBytes));
+            const int k0 = kb * kTcBK;
+            if constexpr (kFwd) {
+              uint64_t keep, stream;
+              asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+              asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
+              tma_load_2d_pair_hint(dA, &jb.tmA, bar, k0, mrow, keep);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if ((hm >> h) & 1u)
+                  tma_load_2d_pair_hint(dB + h * kPKBlockBytes, &jb.tmB, bar, k0,
+                                        jb.v0 + ncol0 + h * kTcBN, stream);
+            } else if (kind == kTcDLogits) {
+              tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if ((hm >> h) & 1u)
+                  tma_load_2d_pair(dB + h * kPKBlockBytes, &jb.tmB, bar, k0,
+                                   jb.v0 + ncol0 + h * kTcBN);
+            } else if (kind == kTcDHidden) {
+              tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if ((hm >> h) & 1u)
+                  tma_load_3d_pair(dB + h * kPKBlockBytes, &jb.tmB, bar, 0, jb.v0 + k0,
+                                   (ncol0 + h * kTcBN) >> 6);
+            } else {
+              tma_load_3d_pair(dA, &jb.tmA, bar, 0, k0, mrow >> 6);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                if ((hm >> h) & 1u)
+                  tma_load_3d_pair(dB + h * kPKBlockBytes, &jb.tmB, bar, 0, k0,
+                                   (ncol0 + h * kTcBN) >> 6);
+            }
+            if (++stage == kPStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          if (++stage == kPStages) {
-            stage = 0;
-            phase ^= 1u;
+        } else {
+          const int ncol = w.tc.n * kTcBN + static_cast<int>(rank) * kPHalf; // this CTA's B columns
+          for (int kb = 0; kb < js[w.job].num_kb; ++kb) {
+            if (!mbar_wait_cl(&empty[stage], phase ^ 1u, abort_flag, a.budget)) {
+              report(st, kStTimeout, 13, t);
+              ok = false;
+              break;
+            }
+            uint8_t* dA = sA + stage * kPABytes;
+            uint8_t* dB = sB + stage * kPBBytes;
+            const uint32_t bar = full_leader0 + 8 * stage;
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * kPStageBytes);
+            constexpr int kblk = kFp8 ? kKbFp8 : kTcBK;      // K of one k-block
+            const int k0 = kb * G::kSub * kblk;
+            if constexpr (kFwd && !kFp8) {
+              uint64_t keep, stream;
+              asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
+              asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
+              tma_load_2d_pair_hint(dA, &jb.tmA, bar, k0, mrow, keep);
+              tma_load_2d_pair_hint(dB, &jb.tmB, bar, k0, jb.v0 + ncol, stream);
+            } else if (kFwd || kMode == 3 || kind == kTcDLogits) {
+#pragma unroll
+              for (int sb = 0; sb < G::kSub; ++sb) {
+                tma_load_2d_pair(dA + sb * kPKBlockBytes, &jb.tmA, bar, k0 + sb * kblk, mrow);
+                tma_load_2d_pair(dB + sb * kPKBlockBytes, &jb.tmB, bar, k0 + sb * kblk,
+                                 jb.v0 + ncol);
+              }
+            } else if (kind == kTcDHidden) {
+              tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
+              tma_load_3d_pair(dB, &jb.tmB, bar, 0, jb.v0 + k0, ncol >> 6);
+            } else {
+              tma_load_3d_pair(dA, &jb.tmA, bar, 0, k0, mrow >> 6);
+              tma_load_3d_pair(dB, &jb.tmB, bar, 0, k0, ncol >> 6);
+            }
+            if (++stage == kPStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
         }
       }
@@ -904,50 +983,121 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
                                             : idesc_bf16_f32(mm, kTcBN, false, false));
         const uint32_t a_lbo = a_mn ? 8192 : 16, a_step = a_mn ? 2048 : 32;
         const uint32_t b_lbo = b_mn ? 8192 : 16, b_step = b_mn ? 2048 : 32;
-        const int buf = it & 1;
-        const uint32_t tph = (it >> 1) & 1;
-        if (!mbar_wait_cl(&tempty[buf], tph ^ 1u, abort_flag, a.budget)) {
-          report(st, kStTimeout, 15, t);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * kTcBN;
-        const int num_kb = js[w.job].num_kb;
-        bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait_cl(&full[stage], phase, abort_flag, a.budget)) {
-            report(st, kStTimeout, 16, t);
-            ok = false;
+        if constexpr (G::kWide) {
+          // TMEM half h of a tile: its epilogue's arrival on tempty[h] frees it
+          // for the next tile (one phase per tile), its last MMA's commit on
+          // tfull[h] hands it to the epilogue
+          const int Kb = js[w.job].num_kb;
+          const bool has1 = 2 * w.tc.n + 1 < js[w.job].num_nb;
+          const int jst = Kb < kWideStagger ? Kb : kWideStagger;
+          const int S = has1 ? Kb + jst : Kb;
+          const uint32_t tph = it & 1;
+          if (!mbar_wait_cl(&tempty[0], tph ^ 1u, abort_flag, a.budget)) {
+            report(st, kStTimeout, 15, t);
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * kPABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * kPBBytes);
-          // four MMAs per 128-byte k-block: K = 16 bf16 or 32 e4m3 each, so
-          // the K-major descriptors advance 32 bytes either way, and a whole
-          // k-block between the k-blocks of a stage
+          bool ok = true;
+          for (int sidx = 0; sidx < S; ++sidx) {
+            const uint32_t hm = !has1 ? 1u : (sidx < jst ? 1u : (sidx < Kb ? 3u : 2u));
+            if (has1 && sidx == jst) {
+              if (!mbar_wait_cl(&tempty[1], tph ^ 1u, abort_flag, a.budget)) {
+                report(st, kStTimeout, 15, t);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+            }
+            if (!mbar_wait_cl(&full[stage], phase, abort_flag, a.budget)) {
+              report(st, kStTimeout, 16, t);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + stage * kPABytes);
+            const uint32_t b_addr = smem_u32(sB + stage * kPBBytes);
 #pragma unroll
-          for (int k = 0; k < 4 * G::kSub; ++k) {
-            const uint32_t kbo = (k / 4) * kPKBlockBytes;
-            const uint64_t adesc = sdesc_sw128(a_addr + kbo + (k % 4) * a_step, a_lbo, 1024);
-            const uint64_t bdesc = sdesc_sw128(b_addr + kbo + (k % 4) * b_step, b_lbo, 1024);
-            if constexpr (kFp8)
-              umma_e4m3_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-            else
-              umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            for (int h = 0; h < 2; ++h) {
+              if (!((hm >> h) & 1u)) continue;
+              const bool first = (h == 0) ? (sidx == 0) : (sidx == jst);
+              const uint32_t d_tmem = tmem_base + h * kTcBN;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const uint64_t adesc = sdesc_sw128(a_addr + k * a_step, a_lbo, 1024);
+                const uint64_t bdesc =
+                    sdesc_sw128(b_addr + h * kPKBlockBytes + k * b_step, b_lbo, 1024);
+                umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (first && k == 0) ? 0u : 1u);
+              }
+            }
+            umma_commit_pair_both(&empty[stage]);
+            if (sidx == Kb - 1) umma_commit_pair_both(&tfull[0]);
+            if (has1 && sidx == S - 1) umma_commit_pair_both(&tfull[1]);
+            if (++stage == kPStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          umma_commit_pair_both(&empty[stage]);
-          if (++stage == kPStages) {
-            stage = 0;
-            phase ^= 1u;
+          if (!ok) break;
+          if (Kb == 0) {
+            mbar_arrive(&tfull[0]);
+            mbar_arrive_cluster(map_rank(&tfull[0], 1));
           }
-        }
-        if (!ok) break;
-        if (num_kb == 0) {
-          mbar_arrive(&tfull[buf]);
-          mbar_arrive_cluster(map_rank(&tfull[buf], 1));
+          if (Kb == 0 || !has1) {
+            // nothing accumulates in half 1: hand it over once its previous
+            // tile's epilogue has released it, keeping one phase per tile
+            if (!mbar_wait_cl(&tempty[1], tph ^ 1u, abort_flag, a.budget)) {
+              report(st, kStTimeout, 15, t);
+              break;
+            }
+            mbar_arrive(&tfull[1]);
+            mbar_arrive_cluster(map_rank(&tfull[1], 1));
+          }
         } else {
-          umma_commit_pair_both(&tfull[buf]);
+          const int buf = it & 1;
+          const uint32_t tph = (it >> 1) & 1;
+          if (!mbar_wait_cl(&tempty[buf], tph ^ 1u, abort_flag, a.budget)) {
+            report(st, kStTimeout, 15, t);
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + buf * kTcBN;
+          const int num_kb = js[w.job].num_kb;
+          bool ok = true;
+          for (int kb = 0; kb < num_kb; ++kb) {
+            if (!mbar_wait_cl(&full[stage], phase, abort_flag, a.budget)) {
+              report(st, kStTimeout, 16, t);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + stage * kPABytes);
+            const uint32_t b_addr = smem_u32(sB + stage * kPBBytes);
+            // four MMAs per 128-byte k-block: K = 16 bf16 or 32 e4m3 each, so
+            // the K-major descriptors advance 32 bytes either way, and a whole
+            // k-block between the k-blocks of a stage
+#pragma unroll
+            for (int k = 0; k < 4 * G::kSub; ++k) {
+              const uint32_t kbo = (k / 4) * kPKBlockBytes;
+              const uint64_t adesc = sdesc_sw128(a_addr + kbo + (k % 4) * a_step, a_lbo, 1024);
+              const uint64_t bdesc = sdesc_sw128(b_addr + kbo + (k % 4) * b_step, b_lbo, 1024);
+              if constexpr (kFp8)
+                umma_e4m3_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+              else
+                umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit_pair_both(&empty[stage]);
+            if (++stage == kPStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (num_kb == 0) {
+            mbar_arrive(&tfull[buf]);
+            mbar_arrive_cluster(map_rank(&tfull[buf], 1));
+          } else {
+            umma_commit_pair_both(&tfull[buf]);
+          }
         }
       }
       umma_commit_pair_local(drain);
@@ -1019,37 +1169,49 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
       } else if (kind == kTcDHidden) {
         active = (tok >= 0) && (a.mask[tok] != 0);
       }
-      if (!mbar_wait_cl(&tfull[buf], tph, abort_flag, a.budget)) {
-        report(st, kStTimeout, 18, t);
-        break;
-      }
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * kTcBN;
-      if constexpr (kMode == 3) {
-        epi_dlogits<true>(jb, tbase, k_empty, r0, w.tc.n, q, row, c0, ncol, rs, sEpi, epi_cnt,
-                          a.wscale);
-      } else if constexpr (kFp8) {
-        epi_fwd<true>(a, tbase, k_empty, r0, w.tc.n, row, tgt, rscale, a.wscale);
-      } else if constexpr (kFwd) {
-        epi_fwd<false>(a, tbase, k_empty, r0, w.tc.n, row, tgt, 0.f, nullptr);
-      } else {
-        if (kind == kTcDLogits)
-          epi_dlogits<false>(jb, tbase, k_empty, r0, w.tc.n, q, row, c0, ncol, rs, sEpi, epi_cnt,
-                             nullptr);
-        else if (kind == kTcDHidden) {
-          if (jb.last_chunk)
-            epi_dhidden_last(a, jb, tbase, k_empty, r0, w.tc.n, row, c0, ncol, tok, active);
-          else
-            epi_dhidden_acc(a, jb, tbase, k_empty, r0, w.tc.n, q, row, c0, ncol, sEpi, epi_cnt);
+      // a wide tile hands over its two halves one after the other (TMEM
+      // columns [0, 256) then [256, 512), one barrier phase per tile each)
+      bool dead = false;
+      for (int h = 0; h < (G::kWide ? 2 : 1); ++h) {
+        const int hb = G::kWide ? h : buf;
+        const uint32_t hph = G::kWide ? (static_cast<uint32_t>(it) & 1u) : tph;
+        if (!mbar_wait_cl(&tfull[hb], hph, abort_flag, a.budget)) {
+          report(st, kStTimeout, 18, t);
+          dead = true;
+          break;
         }
-        else epi_dweight(a, jb, tbase, k_empty, r0, w.tc.n, row);
+        tc_fence_after();
+        const int n_blk = G::kWide ? 2 * w.tc.n + h : w.tc.n;     // 256-column block of N
+        if (!G::kWide || n_blk < js[w.job].num_nb) {
+          const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + hb * kTcBN;
+          if constexpr (kMode == 3) {
+            epi_dlogits<true>(jb, tbase, k_empty, r0, n_blk, q, row, c0, ncol, rs, sEpi, epi_cnt,
+                              a.wscale);
+          } else if constexpr (kFp8) {
+            epi_fwd<true>(a, tbase, k_empty, r0, n_blk, row, tgt, rscale, a.wscale);
+          } else if constexpr (kFwd) {
+            epi_fwd<false>(a, tbase, k_empty, r0, n_blk, row, tgt, 0.f, nullptr);
+          } else {
+            if (kind == kTcDLogits)
+              epi_dlogits<false>(jb, tbase, k_empty, r0, n_blk, q, row, c0, ncol, rs, sEpi, epi_cnt,
+                                 nullptr);
+            else if (kind == kTcDHidden) {
+              if (jb.last_chunk)
+                epi_dhidden_last(a, jb, tbase, k_empty, r0, n_blk, row, c0, ncol, tok, active);
+              else
+                epi_dhidden_acc(a, jb, tbase, k_empty, r0, n_blk, q, row, c0, ncol, sEpi, epi_cnt);
+            }
+            else epi_dweight(a, jb, tbase, k_empty, r0, n_blk, row);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(&tempty[hb]);
+          else mbar_arrive_cluster(tempty_leader0 + 8 * hb);
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(&tempty[buf]);
-        else mbar_arrive_cluster(tempty_leader0 + 8 * buf);
-      }
+      if (dead) break;
     }
     if (!kFwd && lane == 0) bulk_wait_all();   // every staged d-logits box written
   }
