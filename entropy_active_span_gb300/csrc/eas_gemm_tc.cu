@@ -20,28 +20,30 @@
 // the CTA pairs draw from through a global atomic counter, so a pair that
 // finishes early takes more work and the jobs fill each other's tails.
 //
-// Tiles are 256 x 256 and computed by a cluster of two CTAs (the two SMs of a
-// TPC) with tcgen05.mma.cta_group::2: CTA r loads A rows [128r, 128r+128) and
-// B columns [128r, 128r+128) of the tile (32 KB stages of K = 64: seven in the
-// forward, six in the backward, whose epilogues stage their output in the
-// remaining 32 KB and write it with TMA; the e4m3 forward uses three 64 KB
-// stages of two k-blocks).  A K-major operand comes in one 2-D TMA box per
-// k-block, an MN-major one (dHidden's B, dW's A and B) in one 3-D box
-// {64 columns, 64 k-rows, 2 column blocks}, so the producer issues two TMA
-// instructions per k-block whatever the kind.  Each CTA's TMEM receives its
-// 128 x 256 half of the accumulator.  When the last m-tile of a job over the
-// packed rows holds at most 128 real rows, the bf16 backward instantiation
-// (d-logits, dHidden) computes it as a 128 x 256 pair MMA (64 rows per CTA,
+// A cluster of two CTAs (the two SMs of a TPC) computes each tile with
+// tcgen05.mma.cta_group::2: CTA r loads A rows [128r, 128r+128) and, of every
+// 256-column block of B, columns [128r, 128r+128).  The forward and the e4m3
+// kinds compute 256 x 256 tiles: the bf16 forward in seven 32 KB stages of
+// K = 64, the e4m3 ones in three 64 KB stages of two k-blocks; each CTA's
+// TMEM holds two 128 x 256 fp32 accumulators (all 512 columns), so the
+// epilogue of tile i overlaps the mainloop of tile i+1.  The bf16 backward
+// computes 256 x 512 tiles as two staggered 256-column halves in TMEM columns
+// [0, 256) and [256, 512), fed by four 48 KB stages that share each A k-block
+// between the halves (see PipeGeo); its epilogues stage their output in the
+// remaining 32 KB and write it with TMA.  A K-major operand comes in one 2-D
+// TMA box per k-block, an MN-major one (dHidden's B, dW's A and B) in one 3-D
+// box {64 columns, 64 k-rows, 2 column blocks}.  When the last m-tile of a
+// job over the packed rows holds at most 128 real rows, the bf16 backward
+// (d-logits, dHidden) computes it as a 128-row pair MMA (64 rows per CTA,
 // half the tensor time) instead of carrying the padding rows through the
 // tensor pipe; its results are bit-identical to those of a full tile.  CTA
 // layout (192 threads): warp 0 = TMA producer (lane 0; on the even CTA it also
 // fetches tile indices and publishes them to both CTAs), warp 1 = MMA issuer
 // (lane 0 of the even CTA) and TMEM owner, warps 2..5 = epilogue, one
-// accumulator row per thread (warp w reads TMEM lanes 32*(w%4) .. +31).  Two
-// 256-column fp32 accumulators per CTA (all 512 TMEM columns) let the epilogue
-// of tile i overlap the mainloop of tile i+1.  Every mbarrier wait is bounded;
-// on expiry a CTA raises its abort flag, lets its in-flight copies and MMAs
-// land, frees TMEM and reports kStTimeout in the status word.
+// accumulator row per thread (warp w reads TMEM lanes 32*(w%4) .. +31).  Every
+// mbarrier wait is bounded; on expiry a CTA raises its abort flag, lets its
+// in-flight copies and MMAs land, frees TMEM and reports kStTimeout in the
+// status word.
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -499,13 +501,15 @@ __device__ __forceinline__ void epi_dweight(const TcArgs& a, const TcJob& jb, ui
 
 // =====================================================================
 // The CTA-pair kernel.  Against one CTA per 128 x 256 tile, the pair halves
-// the B bytes each SM moves from L2 and reads from shared memory per k-step,
-// and 32 KB stages allow seven of them (224 KB of the 227 KB per CTA).
+// the B bytes each SM moves from L2 and reads from shared memory per k-step.
 //
 // Synchronisation (each line: barrier, where it lives, who arrives):
-//   full[s]   leader   leader producer's expect_tx (64 KB) + both CTAs' TMA bytes
+//   full[s]   leader   leader producer's expect_tx (the stage's bytes of both
+//                      CTAs) + both CTAs' TMA bytes
 //   empty[s]  both     leader MMA commit, multicast to both CTAs
-//   tfull[b]  both     leader MMA commit, multicast to both CTAs
+//   tfull[b]  both     leader MMA commit, multicast to both CTAs (b = the
+//                      tile's parity for 256 x 256 tiles, the half of a wide
+//                      tile)
 //   tempty[b] leader   4 epilogue warps of each CTA (the peer's arrive remotely)
 //   rfull[i]  both     leader fetcher (local arrive + remote arrive)
 //   rempty[i] leader   leader MMA + 4 leader epilogue warps + peer producer
@@ -847,9 +851,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
         const bool half = last_half && a.jobs[w.job].M_fixed <= 0 && w.tc.m == js[w.job].num_m - 1;
         const int mrow = w.tc.m * kPM + static_cast<int>(rank) * (half ? kPHalf / 2 : kPHalf);
         if constexpr (G::kWide) {
-          // k-steps of a wide tile: half 0 alone for k-blocks [0, js), both
-          // halves for [js, Kb), half 1 alone for [0, js); a tile whose second
-          // half lies past N runs half 0 only
+          // k-steps of a wide tile: half 0 alone for k-blocks [0, jst), both
+          // halves for [jst, Kb), half 1 alone for [0, jst); a tile whose
+          // second half lies past N runs half 0 only
           const int Kb = js[w.job].num_kb;
           const bool has1 = 2 * w.tc.n + 1 < js[w.job].num_nb;
           const int jst = Kb < kWideStagger ? Kb : kWideStagger;
@@ -870,17 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_pair_kernel(const __grid_const
             if (leader)
               mbar_arrive_expect_tx(&full[stage], 2u * (kPABytes + nbh * kPKBlockBytes));
             const int k0 = kb * kTcBK;
-            if constexpr (kFwd) {
-              uint64_t keep, stream;
-              asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep));
-              asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(stream));
-              tma_load_2d_pair_hint(dA, &jb.tmA, bar, k0, mrow, keep);
-#pragma unroll
-              for (int h = 0; h < 2; ++h)
-                if ((hm >> h) & 1u)
-                  tma_load_2d_pair_hint(dB + h * kPKBlockBytes, &jb.tmB, bar, k0,
-                                        jb.v0 + ncol0 + h * kTcBN, stream);
-            } else if (kind == kTcDLogits) {
+            if (kind == kTcDLogits) {
               tma_load_2d_pair(dA, &jb.tmA, bar, k0, mrow);
 #pragma unroll
               for (int h = 0; h < 2; ++h)
