@@ -177,6 +177,18 @@ def test_last_row_tile_of_at_most_128_rows(R):
         np.testing.assert_array_equal(got[k][act], dense[k][act])
 
 
+@pytest.mark.parametrize("H,chunk", [(1024, 768), (1088, 1024), (1152, 1088), (960, 1280)])
+def test_wide_tile_k_extents_and_half_tiles(H, chunk):
+    """The backward's 256 x 512 tiles run half 0 alone for the first 16
+    k-blocks, then both halves, then half 1 alone.  K extents of 15, 16, 17
+    and 18 k-blocks (d-logits over H, dHidden over the chunk) cover an empty
+    and a one-step two-half phase; chunk widths of 3 or 5 256-column blocks
+    leave a last wide tile with half 0 only."""
+    inp = small_inputs(300, H, 2100, seed=H + chunk, mask_kind="bernoulli0.7", w_std=3.0)
+    got = run_gpu(inp, vocab_chunk=chunk)
+    check(got, oracle_all(inp), inp["mask"], BF16_TOL)
+
+
 @pytest.mark.parametrize("T,H,V", [(300, 192, 300), (513, 320, 1000), (1, 64, 50), (257, 448, 2049)])
 def test_bf16_hidden_width_not_a_tile_multiple(T, H, V):
     """H % 256 != 0 leaves a partial N tile in dHidden and dW; T = 1 is a
