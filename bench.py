@@ -185,13 +185,12 @@ def _oracle_rows(inp, rows, Wf):
     return time.perf_counter() - t0
 
 
-def oracle_sample_size(inp, Wf, target_s: float, rng) -> int:
-    """Active rows whose oracle fwd+bwd takes about target_s on this host.
-
-    The oracle's time for a batch of n rows is close to a + b*n: a is the
-    part that does not depend on n (its passes over the fp64 copy of W, which
-    dominate small batches), b the per-row work.  Both are fitted from two
-    probe batches of 8 and 64 rows."""
+def oracle_cost_fit(inp, Wf, rng) -> tuple[float, float]:
+    """(a, b) with the oracle's fwd+bwd time for a batch of n active rows
+    close to a + b*n on this host: a is the part that does not depend on n
+    (its passes over the fp64 copy of W, which dominate small batches), b the
+    per-row work.  Fitted from two probe batches of 8 and 64 rows; b = 0 when
+    the workload has no more than 8 active rows."""
     act = np.flatnonzero(inp["mask"])
 
     def probe(n):
@@ -201,10 +200,18 @@ def oracle_sample_size(inp, Wf, target_s: float, rng) -> int:
     n1, t1 = probe(8)
     n2, t2 = probe(64)
     if n2 <= n1:
-        return len(act)
+        return t1, 0.0
     b = max((t2 - t1) / (n2 - n1), 1e-9)
-    a = max(t1 - b * n1, 0.0)
-    return int(max(8, min(len(act), (target_s - a) / b)))
+    return max(t1 - b * n1, 0.0), b
+
+
+def oracle_sample_size(inp, Wf, target_s: float, rng) -> int:
+    """Active rows whose oracle fwd+bwd takes about target_s on this host."""
+    n_act = int(np.count_nonzero(inp["mask"]))
+    a, b = oracle_cost_fit(inp, Wf, rng)
+    if b <= 0.0:
+        return n_act
+    return int(max(8, min(n_act, (target_s - a) / b)))
 
 
 def oracle_sample_rate(inp, target_s: float):
@@ -227,8 +234,14 @@ def reference_arm(args, rank):
     act = np.flatnonzero(inp["mask"])
     Wf = W.to_f64(inp["weight"])
     rng = np.random.default_rng(1)
-    # one step = a sample of active rows sized to about --ref-step-seconds
-    n = oracle_sample_size(inp, Wf, args.ref_step_seconds, rng)
+    # One step = a sample of active rows.  Its target time is --ref-step-seconds
+    # or four times the oracle's per-call fixed cost, whichever is larger, so
+    # that the per-row work dominates the rate; capped so that all warm-up and
+    # timed steps take about three minutes at most.
+    a, b = oracle_cost_fit(inp, Wf, rng)
+    target = max(args.ref_step_seconds, 4.0 * a)
+    target = min(target, max(args.ref_step_seconds, 180.0 / max(1, args.steps + args.warmup)))
+    n = len(act) if b <= 0.0 else int(max(8, min(len(act), (target - a) / b)))
     times = []
     for i in range(args.warmup + args.steps):
         rows = np.sort(rng.choice(act, size=n, replace=False))
